@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the out-of-place transpose on one GB300 (or N replicas).
+
+Default workload: fp32 8192 x 8192 (256 MiB in, 256 MiB out), uniform[-1,1)
+from seed 1, dense pitches.  A step is one whole transpose of that matrix
+through the C ABI (``tr_transpose_ex`` with the AUTO variant).  Inputs and
+outputs are larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line on rank 0:
+  value     effective GB/s = (bytes read + bytes written) / device time, from
+            CUDA events around exactly K back-to-back steps (max over ranks);
+  roofline  the transpose kernel against the measured HBM copy peak;
+  copy      tr_copy on the same byte count, timed the same way (the ceiling);
+  e2e       the same metric with the host->device copy of the input (pinned)
+            and the device->host copy of the output inside every step;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the workload.
+
+``--impl reference`` times the CPU oracle instead (the only other place this
+script runs it) and prints the same line with ``"impl": "reference"``.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from shared_memory_tiled_gb300 import workloads as W  # noqa: E402
+
+METRIC = "transpose effective GB/s (read+write bytes/time) and % of GB300 HBM peak and of copy"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129e6
+
+
+# --------------------------------------------------------------------------- utils
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    """Hash of the sources the timed kernels are built from; a recorded ncu
+    traffic figure is reported only while it still matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shared_memory_tiled_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """dram bytes per launch from the committed ncu summary, or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(kernel_key)
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            return rec.get("dram_bytes_per_launch"), rec.get("scaled_from")
+    except Exception:
+        pass
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names, flags[1:]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world):
+    """Max of a float over all ranks (identity on one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(w, budget_s, max_reps=None, x=None):
+    """Time the oracle on bands of rows of the workload until ``budget_s`` has
+    passed.  Returns (GB/s, seconds, description, reps)."""
+    import numpy as np
+    import oracle
+    if x is None:
+        x = W.make_input(w)
+    out = W.make_output(w)
+    band = min(w.rows, 1024)
+    band_bytes = 2 * w.esize * band * w.cols
+    reps, t_total, r0 = 0, 0.0, 0
+    while True:
+        t = time.perf_counter()
+        oracle.transpose(x[r0 * w.ld_in:], out[r0:], rows=min(band, w.rows - r0), cols=w.cols,
+                         ld_in=w.ld_in, ld_out=w.ld_out)
+        t_total += time.perf_counter() - t
+        reps += 1
+        r0 = (r0 + band) % w.rows
+        done = reps >= max_reps if max_reps else t_total >= budget_s
+        if done:
+            break
+    desc = (f"{reps} oracle transposes of {band}-row bands ({band}x{w.cols}, "
+            f"{band_bytes / 1e6:.1f} MB read+written each) of the {w.name} matrix")
+    return band_bytes * reps / t_total / 1e9, t_total, desc, reps
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    import numpy as np  # noqa: F401
+    x = W.make_input(w)
+    for _ in range(args.warmup):
+        time_oracle(w, 0.0, max_reps=1, x=x)
+    gbs, secs, desc, reps = time_oracle(w, 0.0, max_reps=args.steps, x=x)
+    line = {
+        "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / reps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32" if w.esize == 4 else "u16", "data": "synthetic",
+        "config": {"workload": w.name, "description": W.DESCRIPTION[w.name],
+                   "step": "one 1024-row band of the matrix through the CPU oracle"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from shared_memory_tiled_gb300 import binding as B
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B.load()
+    w = W.WORKLOADS[args.workload]
+    dt = B.DType.F32 if w.esize == 4 else B.DType.BF16
+    tdt = torch.int32 if w.esize == 4 else torch.int16
+    ndt = np.int32 if w.esize == 4 else np.int16
+
+    x_host = W.make_input(w)
+    pin_in = torch.from_numpy(x_host.view(ndt)).pin_memory()
+    pin_out = torch.empty(w.out_elems, dtype=tdt).pin_memory()
+    d_in = torch.empty(w.in_elems, dtype=tdt, device=dev)
+    d_out = torch.empty(w.out_elems, dtype=tdt, device=dev)
+    d_in.copy_(pin_in)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    variant = B.Variant[args.variant.upper()]
+    targs = B.make_args(d_in.data_ptr(), d_out.data_ptr(), dt, w.batch, w.rows, w.cols, w.ld_in,
+                        w.ld_out, w.sin, w.sout, sptr)
+    topts = B.make_options(variant, pad=args.pad, stages=args.stages,
+                           ctas_per_sm=args.ctas_per_sm, tile_order=args.tile_order)
+    planned = B.Variant(B.tr_plan_variant(targs, topts))
+    lib = B.load()
+    ex = lib.tr_transpose_ex
+    import ctypes
+    pa, po = ctypes.byref(targs), ctypes.byref(topts)
+
+    def step():
+        st = ex(pa, po)
+        if st:
+            B.check(st)
+
+    copy_bytes = w.logical_elems * w.esize
+    c_in = torch.empty(copy_bytes, dtype=torch.uint8, device=dev)
+    c_out = torch.empty(copy_bytes, dtype=torch.uint8, device=dev)
+    cfn = lib.tr_copy
+
+    def copy_step():
+        st = cfn(c_in.data_ptr(), c_out.data_ptr(), copy_bytes, sptr)
+        if st:
+            B.check(st)
+
+    def timed(fn, k, warm):
+        for _ in range(warm):
+            fn()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        evs[0].record(stream)
+        for i in range(k):
+            fn()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(k)]
+        total = evs[0].elapsed_time(evs[k])
+        return total, per
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # ---- the timed region: exactly K transposes
+    t_wall0 = time.time()
+    total_ms, per_ms = timed(step, args.steps, args.warmup)
+    t_wall1 = time.time()
+    # keep the same kernel running for ~1 s more if the timed region was too
+    # short for the 100 ms clock samples (the samples then cover this window)
+    extra_window = None
+    if t_wall1 - t_wall0 < 1.0:
+        reps = max(1, int(1.0 / max(statistics.median(per_ms) / 1e3, 1e-6)))
+        tw0 = time.time()
+        timed(step, reps, 0)
+        extra_window = (tw0, time.time())
+    sampler.stop()
+    clocks = sampler.summary(*(extra_window or (t_wall0, t_wall1)))
+    if extra_window:
+        clocks["window"] = "same kernel re-run for 1 s after the timed region"
+
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    gbs = w.algorithmic_bytes * args.steps * world / (total_ms / 1e3) / 1e9
+    med_ms = statistics.median(per_ms)
+    kernel_gbs = w.algorithmic_bytes / (statistics.fmean(per_ms) / 1e3) / 1e9
+
+    # ---- parity guard on the timed output: sampled positions vs the definition
+    got = d_out.cpu().numpy().view(x_host.dtype)
+    rng = np.random.default_rng(123)
+    n = 4096
+    bb = rng.integers(0, w.batch, n)
+    ii = rng.integers(0, w.rows, n)
+    jj = rng.integers(0, w.cols, n)
+    src = x_host[bb * w.sin + ii * w.ld_in + jj]
+    dst = got[bb * w.sout + jj * w.ld_out + ii]
+    if not np.array_equal(src, dst):
+        raise SystemExit("bench: the timed output differs from the input at sampled positions")
+
+    # ---- copy ceiling on the same bytes
+    c_in.random_(0, 255)
+    c_total, c_per = timed(copy_step, args.steps, args.warmup)
+    c_total = max_over_ranks(c_total, world)
+    copy_gbs = 2 * copy_bytes * args.steps / (c_total / 1e3) / 1e9
+
+    # ---- end to end: pinned host input -> device -> transpose -> pinned host output
+    k_e2e = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        d_in.copy_(pin_in, non_blocking=True)
+        step()
+        pin_out.copy_(d_out, non_blocking=True)
+
+    e_total, _ = timed(e2e_step, k_e2e, 2)
+    e_total = max_over_ranks(e_total, world)
+    e2e_gbs = w.algorithmic_bytes * k_e2e * world / (e_total / 1e3) / 1e9
+    if not np.array_equal(pin_out.numpy().view(x_host.dtype)[:64], got[:64]):
+        raise SystemExit("bench: end-to-end output differs from the device-timed output")
+
+    peak, peak_kind = read_peaks()
+    kname = {B.Variant.TMA: "k_tma", B.Variant.TILE_VEC: "k_tile_vec",
+             B.Variant.TILE_PAD: "k_tile_pad"}.get(planned, str(planned.name).lower())
+    traffic, traffic_note = recorded_traffic(f"{kname}:{w.name}")
+
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32" if w.esize == 4 else "u16", "data": "synthetic",
+        "config": {"workload": w.name, "description": W.DESCRIPTION[w.name],
+                   "bytes_per_step": w.algorithmic_bytes, "variant": planned.name,
+                   "l2": "no flush: input and output each larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_measured": round(100 * gbs / world / peak, 2),
+        "pct_of_hbm_nominal": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_copy": round(100 * gbs / (copy_gbs * world), 2),
+        "median_step_ms": round(med_ms, 5),
+        "copy": {"value": round(copy_gbs, 2), "unit": "GB/s", "bytes_per_step": 2 * copy_bytes,
+                 "kernel": "tr_copy"},
+        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
+                     "traffic": traffic, "peak_source": peak_kind, "kernel": kname,
+                     "bytes_per_launch": w.algorithmic_bytes},
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": w.in_elems * w.esize,
+                "d2h_bytes_per_step": w.out_elems * w.esize},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if traffic_note:
+        line["roofline"]["traffic_note"] = traffic_note
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cgbs, csecs, desc, _ = time_oracle(w, args.cpu_seconds, x=x_host)
+        line["cpu_baseline"] = {"value": round(cgbs, 3), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": desc,
+                                "seconds": round(csecs, 2), "host_cpus": os.cpu_count()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(W.WORKLOADS), default="c2")
+    ap.add_argument("--variant", default="auto",
+                    choices=["auto", "naive_row", "naive_col", "tile_pad", "tile_vec", "tma"])
+    ap.add_argument("--pad", type=int, default=1)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--ctas-per-sm", dest="ctas_per_sm", type=int, default=0)
+    ap.add_argument("--tile-order", dest="tile_order", type=int, default=0)
+    ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # never fewer than 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,174 @@
+/*
+ * libtranspose -- out-of-place matrix transpose for GB300 (sm_103a).
+ *
+ * What it computes.  For every batch plane b < batch, input row i < rows and
+ * input column j < cols (all sizes and pitches in ELEMENTS):
+ *
+ *     out[b*stride_out + j*ld_out + i] = in[b*stride_in + i*ld_in + j]
+ *
+ * This is the operation of "Shared memory and the bank conflict"
+ * (roobli.org, kernels-from-zero 03), section "Turn the tile around on chip":
+ * a block reads a tile of the input by rows, turns it around in on-chip shared
+ * memory and writes it out by rows.  "Shared-memory tiling and bank
+ * conflicts" (intro-to-ai-systems-performance, shared-memory chapter),
+ * "Worked example", fixes that global coordinates stay logical and that any
+ * padding lives only in on-chip storage, so the result is the plain transpose
+ * above whatever tile layout a kernel uses.
+ *
+ * Conventions shared by every entry point:
+ *   - Elements are moved as raw bit patterns: the fp32 entry points move
+ *     32-bit words and the bf16 entry points 16-bit words, with no arithmetic
+ *     on them, so NaN payloads, signed zeros and subnormals survive unchanged.
+ *   - rows/cols describe the INPUT plane (rows x cols, row pitch ld_in); the
+ *     output plane is cols x rows with row pitch ld_out.  Required:
+ *     ld_in >= cols, ld_out >= rows.  For batched calls with batch > 1 the
+ *     plane pitches must keep planes apart:
+ *     stride_in >= (rows-1)*ld_in + cols and stride_out >= (cols-1)*ld_out + rows.
+ *   - Only the logical output elements are written; pitch padding of the
+ *     output keeps whatever it held.
+ *   - `in` and `out` are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory in any call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and do not synchronize.
+ *   - A zero dimension returns TR_OK without launching anything.  A negative
+ *     dimension returns TR_ERR_BAD_DIM, a pitch below its minimum
+ *     TR_ERR_BAD_LD, a NULL pointer with a nonzero size TR_ERR_NULL, and any
+ *     byte overlap between the input and output extents TR_ERR_OVERLAP (the
+ *     operation is out-of-place).  Argument errors are detected on the host
+ *     before any CUDA call.
+ *   - A CUDA launch or driver failure returns TR_ERR_CUDA; tr_last_error()
+ *     then describes it (per host thread).
+ *   - Every wait on an mbarrier inside a kernel is bounded.  A wait that runs
+ *     out records a device-side fault flag and the kernel returns early;
+ *     tr_device_status() reports it as TR_ERR_TIMEOUT.
+ */
+#ifndef LIBTRANSPOSE_TRANSPOSE_H
+#define LIBTRANSPOSE_TRANSPOSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *tr_stream_t;
+
+typedef enum tr_status {
+    TR_OK = 0,
+    TR_ERR_NULL = 1,         /* NULL pointer with a nonzero size                       */
+    TR_ERR_BAD_DIM = 2,      /* negative size, or a size/extent that overflows int64   */
+    TR_ERR_BAD_LD = 3,       /* row or plane pitch below its minimum                   */
+    TR_ERR_OVERLAP = 4,      /* input and output byte extents overlap                  */
+    TR_ERR_UNSUPPORTED = 5,  /* requested variant cannot run on these arguments        */
+    TR_ERR_CUDA = 6,         /* CUDA runtime/driver error; see tr_last_error()         */
+    TR_ERR_TIMEOUT = 7       /* a bounded in-kernel wait ran out (tr_device_status)    */
+} tr_status;
+
+/* Element width of a transpose. */
+typedef enum tr_dtype {
+    TR_DTYPE_F32 = 0,        /* 4-byte elements (fp32 bit patterns)  */
+    TR_DTYPE_BF16 = 1        /* 2-byte elements (bf16 bit patterns)  */
+} tr_dtype;
+
+/* Kernel variants.  All give bit-identical results; they differ in how the
+ * tile is staged.  AUTO picks the fastest one the arguments allow. */
+typedef enum tr_variant {
+    TR_VARIANT_AUTO = 0,
+    /* One element per thread, no shared memory; reads coalesced, writes strided
+     * down a column ("episode 02" of the kernels-from-zero series). */
+    TR_VARIANT_NAIVE_ROW = 1,
+    /* One element per thread, no shared memory; reads strided, writes coalesced. */
+    TR_VARIANT_NAIVE_COL = 2,
+    /* 32 x 32 tile, 32 x 8 threads, one element per access, shared row pitch of
+     * 32 + pad elements ("Shared memory and the bank conflict", kernel
+     * transpose_tiled; pad = 0 is its unpadded width-32 form). */
+    TR_VARIANT_TILE_PAD = 3,
+    /* 16-byte global loads and stores, XOR-swizzled shared tile read with
+     * 16-byte accesses, register micro-transpose (4x4 fp32, 8x8 bf16). */
+    TR_VARIANT_TILE_VEC = 4,
+    /* TMA tile loads and stores with the hardware 128-byte swizzle, persistent
+     * CTAs and an mbarrier pipeline.  Needs 16-byte aligned bases and pitches. */
+    TR_VARIANT_TMA = 5
+} tr_variant;
+
+/* Tuning knobs for tr_transpose_ex.  Zero-initialise for defaults. */
+typedef struct tr_options {
+    int32_t variant;      /* tr_variant                                                  */
+    int32_t pad;          /* TILE_PAD: shared row pitch is 32 + pad elements, 0..8        */
+    int32_t ctas_per_sm;  /* TMA: persistent CTAs per SM, 0 = as many as fit (max 8)      */
+    int32_t stages;       /* TMA: input pipeline depth 2..8, 0 = default                  */
+    int32_t tile_order;   /* TMA/TILE_VEC: 0 = row-major tile walk, 1 = diagonal          */
+    int32_t reserved[3];  /* must be zero                                                 */
+} tr_options;
+
+/* Full argument set of one (possibly batched) transpose; see the conventions
+ * above.  For a single matrix set batch = 1 (stride_in/stride_out ignored). */
+typedef struct tr_args {
+    const void *in;
+    void *out;
+    int32_t dtype;        /* tr_dtype */
+    int32_t reserved;     /* must be zero */
+    int64_t batch, rows, cols;
+    int64_t ld_in, ld_out;
+    int64_t stride_in, stride_out;
+    tr_stream_t stream;
+} tr_args;
+
+/* Single-matrix transpose of fp32 bit patterns (rows x cols -> cols x rows). */
+tr_status tr_transpose_f32(const float *in, float *out, int64_t rows, int64_t cols,
+                           int64_t ld_in, int64_t ld_out, tr_stream_t stream);
+
+/* Single-matrix transpose of bf16 bit patterns (`in`/`out` point at 16-bit elements). */
+tr_status tr_transpose_bf16(const void *in, void *out, int64_t rows, int64_t cols,
+                            int64_t ld_in, int64_t ld_out, tr_stream_t stream);
+
+/* Batched transpose [batch, rows, cols] -> [batch, cols, rows] of fp32 bit
+ * patterns; plane b of the input starts at in + b*stride_in, of the output at
+ * out + b*stride_out (elements). */
+tr_status tr_transpose_batched_f32(const float *in, float *out, int64_t batch, int64_t rows,
+                                   int64_t cols, int64_t ld_in, int64_t ld_out,
+                                   int64_t stride_in, int64_t stride_out, tr_stream_t stream);
+
+/* Batched transpose of bf16 bit patterns; same arguments as the fp32 form. */
+tr_status tr_transpose_batched_bf16(const void *in, void *out, int64_t batch, int64_t rows,
+                                    int64_t cols, int64_t ld_in, int64_t ld_out,
+                                    int64_t stride_in, int64_t stride_out, tr_stream_t stream);
+
+/* Any transpose with an explicit variant and tuning (opts may be NULL = AUTO).
+ * Returns TR_ERR_UNSUPPORTED when the requested variant cannot run on these
+ * arguments (e.g. TMA with a pitch that is not a multiple of 16 bytes). */
+tr_status tr_transpose_ex(const tr_args *args, const tr_options *opts);
+
+/* Device-to-device copy of `bytes` bytes, the bandwidth ceiling the transpose
+ * is compared against ("Shared memory and the bank conflict", section "What to
+ * record": the transpose timings sit next to a copy of the same bytes).
+ * Any alignment; the ranges must not overlap (TR_ERR_OVERLAP). */
+tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream);
+
+/* Host-only planning: the variant tr_transpose_ex would run for these
+ * arguments and options (a tr_variant value, never AUTO), or a negative
+ * tr_status on invalid arguments.  Makes no CUDA call. */
+int32_t tr_plan_variant(const tr_args *args, const tr_options *opts);
+
+/* Reads and clears the device-side fault flag of the CURRENT device after
+ * synchronizing it: TR_ERR_TIMEOUT if a bounded in-kernel wait ran out since
+ * the last call, TR_OK otherwise (TR_ERR_CUDA if the read itself fails). */
+tr_status tr_device_status(void);
+
+/* Static description of a status code (never NULL). */
+const char *tr_status_string(tr_status status);
+
+/* Description of the last TR_ERR_CUDA / TR_ERR_UNSUPPORTED on this host
+ * thread, or "" (never NULL; valid until the next call on this thread). */
+const char *tr_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t tr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBTRANSPOSE_TRANSPOSE_H */

@@ -1,0 +1,287 @@
+// The C-ABI boundary of libtranspose: argument validation, variant choice and
+// dispatch to the kernel launchers.  Everything here runs on the host; the
+// validation and planning functions make no CUDA call, so argument errors are
+// reported without a GPU.
+#include "tr_internal.h"
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace tr {
+namespace {
+
+thread_local std::string t_last_error;
+
+void set_error(const char *what, cudaError_t e) {
+    char buf[512];
+    if (e != cudaSuccess)
+        std::snprintf(buf, sizeof buf, "%s: %s (%s)", what, cudaGetErrorName(e),
+                      cudaGetErrorString(e));
+    else
+        std::snprintf(buf, sizeof buf, "%s", what);
+    t_last_error = buf;
+}
+
+// a*b + c with overflow detection; all inputs non-negative.
+bool mul_add(int64_t a, int64_t b, int64_t c, int64_t *r) {
+    __int128 v = (__int128)a * b + c;
+    if (v > INT64_MAX) return false;
+    *r = int64_t(v);
+    return true;
+}
+
+// Elements from the first to one past the last logical element of a side.
+bool side_extent(int64_t batch, int64_t lines, int64_t elems, int64_t ld, int64_t stride,
+                 int64_t *ext) {
+    if (batch == 0 || lines == 0 || elems == 0) {
+        *ext = 0;
+        return true;
+    }
+    int64_t e1, e2;
+    if (!mul_add(lines - 1, ld, elems, &e1)) return false;
+    if (!mul_add(batch - 1, stride, e1, &e2)) return false;
+    *ext = e2;
+    return true;
+}
+
+// Validates the arguments and fills a Problem.  Returns TR_OK, an argument
+// error, or (via *empty) that there is nothing to do.
+tr_status validate(const tr_args *a, Problem *p, bool *empty) {
+    if (!a) return TR_ERR_NULL;
+    if (a->reserved != 0) return TR_ERR_UNSUPPORTED;
+    if (a->dtype != TR_DTYPE_F32 && a->dtype != TR_DTYPE_BF16) return TR_ERR_UNSUPPORTED;
+    if (a->batch < 0 || a->rows < 0 || a->cols < 0) return TR_ERR_BAD_DIM;
+    const int esize = a->dtype == TR_DTYPE_F32 ? 4 : 2;
+    *empty = a->batch == 0 || a->rows == 0 || a->cols == 0;
+    if (*empty) return TR_OK;
+    if (!a->in || !a->out) return TR_ERR_NULL;
+    if (a->ld_in < a->cols || a->ld_out < a->rows) return TR_ERR_BAD_LD;
+    int64_t min_sin, min_sout;
+    if (!mul_add(a->rows - 1, a->ld_in, a->cols, &min_sin) ||
+        !mul_add(a->cols - 1, a->ld_out, a->rows, &min_sout))
+        return TR_ERR_BAD_DIM;
+    if (a->batch > 1 && (a->stride_in < min_sin || a->stride_out < min_sout)) return TR_ERR_BAD_LD;
+    int64_t ext_in, ext_out, bytes_in, bytes_out;
+    if (!side_extent(a->batch, a->rows, a->cols, a->ld_in, a->stride_in, &ext_in) ||
+        !side_extent(a->batch, a->cols, a->rows, a->ld_out, a->stride_out, &ext_out) ||
+        !mul_add(ext_in, esize, 0, &bytes_in) || !mul_add(ext_out, esize, 0, &bytes_out))
+        return TR_ERR_BAD_DIM;
+    const uintptr_t i0 = reinterpret_cast<uintptr_t>(a->in);
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(a->out);
+    if (i0 + uintptr_t(bytes_in) < i0 || o0 + uintptr_t(bytes_out) < o0) return TR_ERR_BAD_DIM;
+    if (i0 < o0 + uintptr_t(bytes_out) && o0 < i0 + uintptr_t(bytes_in)) return TR_ERR_OVERLAP;
+    p->in = a->in;
+    p->out = a->out;
+    p->esize = esize;
+    p->batch = a->batch;
+    p->rows = a->rows;
+    p->cols = a->cols;
+    p->ld_in = a->ld_in;
+    p->ld_out = a->ld_out;
+    p->stride_in = a->batch > 1 ? a->stride_in : a->rows * a->ld_in;
+    p->stride_out = a->batch > 1 ? a->stride_out : a->cols * a->ld_out;
+    p->stream = reinterpret_cast<cudaStream_t>(a->stream);
+    return TR_OK;
+}
+
+bool options_valid(const tr_options *o) {
+    if (!o) return true;
+    if (o->variant < TR_VARIANT_AUTO || o->variant > TR_VARIANT_TMA) return false;
+    if (o->pad < 0 || o->pad > 8 || (o->pad > 4 && o->pad != 8)) return false;
+    if (o->ctas_per_sm < 0 || o->ctas_per_sm > 8) return false;
+    if (o->stages != 0 && (o->stages < 2 || o->stages > 8)) return false;
+    if (o->tile_order < 0 || o->tile_order > 1) return false;
+    for (int r : o->reserved)
+        if (r != 0) return false;
+    return true;
+}
+
+// Variant choice (host logic only).  AUTO takes TMA when both sides allow
+// 16-byte aligned tiles, else the vectorised LSU tile, which itself falls back
+// to single-element global accesses on a misaligned side.
+int32_t choose(const Problem &p, const tr_options *o) {
+    const int req = o ? o->variant : TR_VARIANT_AUTO;
+    if (req != TR_VARIANT_AUTO) return req;
+    const bool in16 = side_aligned16(p.in, p.ld_in, p.stride_in, p.batch, p.esize);
+    const bool out16 = side_aligned16(p.out, p.ld_out, p.stride_out, p.batch, p.esize);
+    if (in16 && out16) return TR_VARIANT_TMA;
+    return TR_VARIANT_TILE_VEC;
+}
+
+tr_status run(const tr_args *a, const tr_options *o) {
+    Problem p{};
+    bool empty = false;
+    if (!options_valid(o)) return TR_ERR_UNSUPPORTED;
+    tr_status st = validate(a, &p, &empty);
+    if (st != TR_OK || empty) return st;
+    const int32_t v = choose(p, o);
+    const bool in16 = side_aligned16(p.in, p.ld_in, p.stride_in, p.batch, p.esize);
+    const bool out16 = side_aligned16(p.out, p.ld_out, p.stride_out, p.batch, p.esize);
+    cudaError_t e = cudaSuccess;
+    switch (v) {
+        case TR_VARIANT_NAIVE_ROW: e = launch_naive(p, true); break;
+        case TR_VARIANT_NAIVE_COL: e = launch_naive(p, false); break;
+        case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
+        case TR_VARIANT_TILE_VEC: e = launch_tile_vec(p, in16, out16, o ? o->tile_order : 0); break;
+        case TR_VARIANT_TMA: {
+            if (!in16 || !out16) {
+                set_error("TMA needs 16-byte aligned base pointers and pitches on both sides",
+                          cudaSuccess);
+                return TR_ERR_UNSUPPORTED;
+            }
+            TmaConfig cfg{o ? o->ctas_per_sm : 0, o ? o->stages : 0, o ? o->tile_order : 0};
+            const char *why = nullptr;
+            e = launch_tma(p, cfg, &why);
+            if (e != cudaSuccess && why) {
+                const bool auto_mode = !o || o->variant == TR_VARIANT_AUTO;
+                if (auto_mode) {
+                    // The planner's first choice could not be encoded (e.g. a
+                    // plane pitch the tensor map rejects): take the LSU tile.
+                    e = launch_tile_vec(p, in16, out16, cfg.tile_order);
+                    break;
+                }
+                set_error(why, cudaSuccess);
+                return TR_ERR_UNSUPPORTED;
+            }
+            break;
+        }
+        default: return TR_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) {
+        set_error("kernel launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
+tr_args make_args(const void *in, void *out, tr_dtype dt, int64_t batch, int64_t rows,
+                  int64_t cols, int64_t ld_in, int64_t ld_out, int64_t stride_in,
+                  int64_t stride_out, tr_stream_t stream) {
+    tr_args a{};
+    a.in = in;
+    a.out = out;
+    a.dtype = dt;
+    a.batch = batch;
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_in = ld_in;
+    a.ld_out = ld_out;
+    a.stride_in = stride_in;
+    a.stride_out = stride_out;
+    a.stream = stream;
+    return a;
+}
+
+}  // namespace
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace tr
+
+extern "C" {
+
+tr_status tr_transpose_f32(const float *in, float *out, int64_t rows, int64_t cols, int64_t ld_in,
+                           int64_t ld_out, tr_stream_t stream) {
+    const tr_args a = tr::make_args(in, out, TR_DTYPE_F32, 1, rows, cols, ld_in, ld_out, 0, 0, stream);
+    return tr::run(&a, nullptr);
+}
+
+tr_status tr_transpose_bf16(const void *in, void *out, int64_t rows, int64_t cols, int64_t ld_in,
+                            int64_t ld_out, tr_stream_t stream) {
+    const tr_args a = tr::make_args(in, out, TR_DTYPE_BF16, 1, rows, cols, ld_in, ld_out, 0, 0, stream);
+    return tr::run(&a, nullptr);
+}
+
+tr_status tr_transpose_batched_f32(const float *in, float *out, int64_t batch, int64_t rows,
+                                   int64_t cols, int64_t ld_in, int64_t ld_out, int64_t stride_in,
+                                   int64_t stride_out, tr_stream_t stream) {
+    const tr_args a = tr::make_args(in, out, TR_DTYPE_F32, batch, rows, cols, ld_in, ld_out,
+                                    stride_in, stride_out, stream);
+    return tr::run(&a, nullptr);
+}
+
+tr_status tr_transpose_batched_bf16(const void *in, void *out, int64_t batch, int64_t rows,
+                                    int64_t cols, int64_t ld_in, int64_t ld_out, int64_t stride_in,
+                                    int64_t stride_out, tr_stream_t stream) {
+    const tr_args a = tr::make_args(in, out, TR_DTYPE_BF16, batch, rows, cols, ld_in, ld_out,
+                                    stride_in, stride_out, stream);
+    return tr::run(&a, nullptr);
+}
+
+tr_status tr_transpose_ex(const tr_args *args, const tr_options *opts) {
+    return tr::run(args, opts);
+}
+
+tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream) {
+    if (bytes == 0) return TR_OK;
+    if (!in || !out) return TR_ERR_NULL;
+    if (bytes > size_t(INT64_MAX)) return TR_ERR_BAD_DIM;
+    const uintptr_t i0 = reinterpret_cast<uintptr_t>(in), o0 = reinterpret_cast<uintptr_t>(out);
+    if (i0 + bytes < i0 || o0 + bytes < o0) return TR_ERR_BAD_DIM;
+    if (i0 < o0 + bytes && o0 < i0 + bytes) return TR_ERR_OVERLAP;
+    const cudaError_t e = tr::launch_copy(in, out, bytes, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tr::set_error("copy launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
+int32_t tr_plan_variant(const tr_args *args, const tr_options *opts) {
+    tr::Problem p{};
+    bool empty = false;
+    if (!tr::options_valid(opts)) return -int32_t(TR_ERR_UNSUPPORTED);
+    const tr_status st = tr::validate(args, &p, &empty);
+    if (st != TR_OK) return -int32_t(st);
+    if (empty) {
+        // Nothing would launch; report the choice for the same pointers and pitches.
+        p = tr::Problem{args->in, args->out, args->dtype == TR_DTYPE_F32 ? 4 : 2, args->batch,
+                        args->rows, args->cols, args->ld_in, args->ld_out, args->stride_in,
+                        args->stride_out, nullptr};
+    }
+    return tr::choose(p, opts);
+}
+
+tr_status tr_device_status(void) {
+    unsigned v = 0;
+    const cudaError_t e = tr::read_and_clear_fault(&v);
+    if (e != cudaSuccess) {
+        tr::set_error("reading the device fault flag failed", e);
+        return TR_ERR_CUDA;
+    }
+    return v ? TR_ERR_TIMEOUT : TR_OK;
+}
+
+const char *tr_status_string(tr_status s) {
+    switch (s) {
+        case TR_OK: return "success";
+        case TR_ERR_NULL: return "NULL pointer with a nonzero size";
+        case TR_ERR_BAD_DIM: return "negative or overflowing dimension";
+        case TR_ERR_BAD_LD: return "row or plane pitch below its minimum";
+        case TR_ERR_OVERLAP: return "input and output ranges overlap";
+        case TR_ERR_UNSUPPORTED: return "variant or option not supported for these arguments";
+        case TR_ERR_CUDA: return "CUDA error (see tr_last_error)";
+        case TR_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    }
+    return "unknown status";
+}
+
+const char *tr_last_error(void) { return tr::t_last_error.c_str(); }
+
+int32_t tr_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+}  // extern "C"

@@ -1,0 +1,323 @@
+// TMA transpose: tiles move between global and shared memory with
+// cp.async.bulk.tensor in the hardware's 128-byte swizzle, and the threads only
+// turn each tile around on chip.
+//
+// Tile: 16V x 16V elements with V = 16 / sizeof(T) elements per 16-byte chunk
+// (64x64 fp32, 128x128 bf16).  TMA boxes are 128 bytes wide (the widest box
+// the 128-byte swizzle allows), so an input tile arrives as two boxes of 16V
+// rows x 8 chunks (input columns 0..8V-1 and 8V..16V-1) and the output tile
+// leaves as two boxes of 16V output rows x 8 chunks (input rows 0..8V-1 and
+// 8V..16V-1).  In a 1024-byte aligned box with 128-byte rows the swizzle puts
+// chunk k of row r at chunk position k ^ (r % 8).
+//
+// Each of the 256 threads owns one V x V micro-block: tile rows V*A..V*A+V-1
+// (A < 16) and chunk C (< 16).  It reads V chunks with 16-byte shared loads,
+// transposes them in registers (pure renaming for fp32, byte permutes for
+// bf16) and writes V chunks of the output tile.  With a = A % 8, c = C % 8:
+//   read  row V*A+m, chunk c   -> position c ^ ((V*A+m) % 8)
+//   write row V*C+m', chunk a  -> position a ^ ((V*C+m') % 8)
+// A 16-byte shared access is served 8 lanes at a time, and is conflict-free
+// when those 8 lanes hit 8 distinct positions.  The 8 lanes of one phase take
+// the micro-blocks (a, c) = (x ^ s, x), x = 0..7, for one s: for bf16 both
+// maps reduce to c ^ m and a ^ m' (distinct because c and a are); for fp32
+// they are x ^ 4*((x^s) & 1) ^ m and x ^ s ^ 4*(x & 1) ^ m', each a bijection
+// of x.  So every shared access of the kernel is conflict-free.
+//
+// Pipeline (per persistent CTA, tiles blockIdx.x, +gridDim.x, ...):
+//   thread 0 keeps up to `in_stages` tile loads in flight, one mbarrier per
+//   input slot (arrive.expect_tx + complete_tx);  all threads wait for the
+//   slot's phase, transpose into one of two output buffers, fence the async
+//   proxy and meet at one CTA barrier; thread 0 then issues the TMA store of
+//   the output buffer, refills the input slot and, before the next barrier,
+//   waits until the store issued two tiles ago has finished reading its
+//   buffer ("Shared-memory tiling and bank conflicts", "Protect tile phases":
+//   a buffer is reusable only after its readers finish).
+// Every mbarrier wait is bounded; a wait that runs out sets the device fault
+// flag, the CTA drains the copies it has in flight and returns.
+#include "ptx.cuh"
+#include "tr_internal.h"
+
+#include <cstdio>
+#include <mutex>
+
+namespace tr {
+
+// Set when a bounded in-kernel wait ran out; read and cleared by the host.
+__device__ unsigned g_fault_flag = 0;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kOutStages = 2;
+
+struct TmaGeom {
+    int64_t total;        // batch * tiles_r * tiles_c
+    int32_t tiles_r, tiles_c;
+    int32_t rows;         // input rows (= output columns) for store clipping
+    int32_t in_stages;
+    int32_t diagonal;
+};
+
+template <typename T>
+struct TmaTile {
+    static constexpr int V = 16 / int(sizeof(T));
+    static constexpr int TILE = 16 * V;             // elements per tile side
+    static constexpr int BOXC = 8 * V;              // elements per 128-byte box row
+    static constexpr int BOX_BYTES = TILE * 128;    // one box: TILE rows x 128 bytes
+    static constexpr int BUF_BYTES = 2 * BOX_BYTES; // one tile
+};
+
+__device__ __forceinline__ void tile_coords(const TmaGeom &g, int64_t t, int32_t &b, int32_t &tr,
+                                            int32_t &tc) {
+    const int64_t per_plane = int64_t(g.tiles_r) * g.tiles_c;
+    const int64_t bb = t / per_plane;
+    const int64_t r = t - bb * per_plane;
+    int64_t r_ = r / g.tiles_c;
+    int64_t c_ = r - r_ * g.tiles_c;
+    if (g.diagonal) {
+        c_ += r_;
+        c_ %= g.tiles_c;
+    }
+    b = int32_t(bb);
+    tr = int32_t(r_);
+    tc = int32_t(c_);
+}
+
+__device__ __forceinline__ void micro_transpose(const uint4 (&x)[4], uint4 (&y)[4]) {
+    y[0] = make_uint4(x[0].x, x[1].x, x[2].x, x[3].x);
+    y[1] = make_uint4(x[0].y, x[1].y, x[2].y, x[3].y);
+    y[2] = make_uint4(x[0].z, x[1].z, x[2].z, x[3].z);
+    y[3] = make_uint4(x[0].w, x[1].w, x[2].w, x[3].w);
+}
+
+// 8x8 transpose of 16-bit elements: output row m takes half (m & 1) of word
+// (m >> 1) of every input row; output word w pairs input rows 2w and 2w+1.
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ void micro_transpose(const uint4 (&x)[8], uint4 (&y)[8]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
+        const int k = m >> 1;
+        y[m] = make_uint4(__byte_perm(word_of(x[0], k), word_of(x[1], k), sel),
+                          __byte_perm(word_of(x[2], k), word_of(x[3], k), sel),
+                          __byte_perm(word_of(x[4], k), word_of(x[5], k), sel),
+                          __byte_perm(word_of(x[6], k), word_of(x[7], k), sel));
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
+      TmaGeom g) {
+    using L = TmaTile<T>;
+    constexpr int V = L::V;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *in_buf = base;
+    uint8_t *out_buf = base + size_t(g.in_stages) * L::BUF_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_buf + kOutStages * L::BUF_BYTES);
+
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int quad = w >> 1;                      // which 8x8 group of micro-blocks
+    const int s = (lane >> 3) + 4 * (w & 1);      // generalized diagonal of the phase
+    const int c = lane & 7, a = c ^ s;
+    const int A = 8 * (quad >> 1) + a, C = 8 * (quad & 1) + c;
+    uint32_t roff[V], woff[V];
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const int r = V * A + m, o = V * C + m;
+        roff[m] = (C >> 3) * L::BOX_BYTES + r * 128 + ((c ^ (r & 7)) << 4);
+        woff[m] = (A >> 3) * L::BOX_BYTES + o * 128 + ((a ^ (o & 7)) << 4);
+    }
+
+    const int64_t n_local =
+        blockIdx.x < g.total ? (g.total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int S = g.in_stages;
+
+    auto issue_load = [&](int64_t k, int slot) {
+        int32_t b, tr, tc;
+        tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
+        uint64_t *bar = full + slot;
+        ptx::mbar_arrive_expect_tx(bar, L::BUF_BYTES);
+        uint8_t *dst = in_buf + size_t(slot) * L::BUF_BYTES;
+        ptx::tma_load_3d(dst, &tm_in, bar, tc * L::TILE, tr * L::TILE, b);
+        ptx::tma_load_3d(dst + L::BOX_BYTES, &tm_in, bar, tc * L::TILE + L::BOXC, tr * L::TILE, b);
+    };
+
+    if (t == 0) {
+        ptx::prefetch_tensormap(&tm_in);
+        ptx::prefetch_tensormap(&tm_out);
+        for (int i = 0; i < S; ++i) ptx::mbar_init(full + i, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (t == 0)
+        for (int64_t k = 0; k < n_local && k < S; ++k) issue_load(k, int(k));
+
+    int64_t k = 0;
+    bool aborted = false;
+    for (; k < n_local; ++k) {
+        const int slot = int(k % S);
+        const uint32_t parity = uint32_t((k / S) & 1);
+        const bool ok = ptx::mbar_wait_bounded(full + slot, parity);
+
+        const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
+        uint8_t *ob = out_buf + size_t(k & 1) * L::BUF_BYTES;
+        uint4 x[V], y[V];
+#pragma unroll
+        for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
+        micro_transpose(x, y);
+#pragma unroll
+        for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[m]) = y[m];
+        ptx::fence_proxy_async_smem();
+        // The store issued for tile k-1 must finish reading its buffer before
+        // tile k+1 is written there (two output buffers).
+        if (t == 0) ptx::bulk_wait_group_read<kOutStages - 2>();
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        if (t == 0) {
+            int32_t b, tr, tc;
+            tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
+            ptx::tma_store_3d(&tm_out, ob, tr * L::TILE, tc * L::TILE, b);
+            if (tr * L::TILE + L::BOXC < g.rows)
+                ptx::tma_store_3d(&tm_out, ob + L::BOX_BYTES, tr * L::TILE + L::BOXC, tc * L::TILE,
+                                  b);
+            ptx::bulk_commit_group();
+            if (k + S < n_local) issue_load(k + S, slot);
+        }
+    }
+
+    if (t == 0) {
+        if (aborted) {
+            atomicExch(&g_fault_flag, 1u);
+            // Drain the loads still in flight (tiles k .. k+S-1) before the
+            // shared memory they target goes away; each wait is bounded too.
+            for (int64_t kk = k; kk < n_local && kk < k + S; ++kk)
+                ptx::mbar_wait_bounded(full + int(kk % S), uint32_t((kk / S) & 1));
+        }
+        ptx::bulk_wait_group<0>();
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D map over [planes][lines][elems] with a 128-byte-wide box of box_lines lines.
+bool encode_3d(CUtensorMap *map, const void *base, int esize, int64_t elems, int64_t lines,
+               int64_t planes, int64_t line_pitch, int64_t plane_pitch, int box_elems,
+               int box_lines) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(elems), cuuint64_t(lines), cuuint64_t(planes)};
+    const cuuint64_t strides[2] = {cuuint64_t(line_pitch) * esize,
+                                   cuuint64_t(plane_pitch) * esize};
+    const cuuint32_t box[3] = {cuuint32_t(box_elems), cuuint32_t(box_lines), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                          3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T>
+cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **why) {
+    using L = TmaTile<T>;
+    const int64_t two31 = int64_t(1) << 31, two40 = int64_t(1) << 40;
+    if (p.rows >= two31 || p.cols >= two31 || p.batch >= two31) {
+        *why = "TMA coordinates are 32-bit: a dimension is 2^31 or more";
+        return cudaErrorInvalidValue;
+    }
+    // Plane pitches as the tensor map sees them: a single plane still needs a
+    // legal third-dimension stride, and it must cover a whole plane.
+    const int64_t sin = p.batch > 1 ? p.stride_in : p.rows * p.ld_in;
+    const int64_t sout = p.batch > 1 ? p.stride_out : p.cols * p.ld_out;
+    if (sin < p.rows * p.ld_in || sout < p.cols * p.ld_out || sin * p.esize >= two40 ||
+        sout * p.esize >= two40 || p.ld_in * p.esize >= two40 || p.ld_out * p.esize >= two40) {
+        *why = "TMA needs plane pitches that cover whole planes and strides below 2^40 bytes";
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap tm_in, tm_out;
+    if (!encode_3d(&tm_in, p.in, p.esize, p.cols, p.rows, p.batch, p.ld_in, sin, L::BOXC,
+                   L::TILE) ||
+        !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, L::BOXC,
+                   L::TILE)) {
+        *why = "cuTensorMapEncodeTiled rejected the tensor maps";
+        return cudaErrorInvalidValue;
+    }
+    TmaGeom g{};
+    g.tiles_r = int32_t((p.rows + L::TILE - 1) / L::TILE);
+    g.tiles_c = int32_t((p.cols + L::TILE - 1) / L::TILE);
+    g.total = p.batch * int64_t(g.tiles_r) * g.tiles_c;
+    g.rows = int32_t(p.rows);
+    g.diagonal = cfg.tile_order == 1;
+    int stages = cfg.stages > 0 ? cfg.stages : (sizeof(T) == 4 ? 4 : 3);
+    if (stages < 2) stages = 2;
+    if (stages > 8) stages = 8;
+    g.in_stages = stages;
+    const size_t smem = 1024 + size_t(stages + kOutStages) * L::BUF_BYTES + size_t(stages) * 8;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int max_optin = 0;
+    e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if (smem > size_t(max_optin)) {
+        *why = "TMA pipeline does not fit in shared memory; lower the stage count";
+        return cudaErrorInvalidValue;
+    }
+    e = cudaFuncSetAttribute(k_tma<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    int fit = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma<T>, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (fit < 1) {
+        *why = "TMA kernel cannot be resident with this configuration";
+        return cudaErrorInvalidValue;
+    }
+    int per_sm = cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : fit;
+    if (per_sm > fit) per_sm = fit;
+    int64_t grid = int64_t(sm_count()) * per_sm;
+    if (grid > g.total) grid = g.total;
+    k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tma(const Problem &p, const TmaConfig &cfg, const char **why) {
+    return p.esize == 4 ? launch_typed<uint32_t>(p, cfg, why) : launch_typed<uint16_t>(p, cfg, why);
+}
+
+cudaError_t read_and_clear_fault(unsigned *value) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_fault_flag, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_fault_flag, &zero, sizeof(unsigned));
+}
+
+}  // namespace tr

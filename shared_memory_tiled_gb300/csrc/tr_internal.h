@@ -1,0 +1,53 @@
+// Internal declarations shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "transpose.h"
+
+namespace tr {
+
+// One validated transpose problem (sizes and pitches in elements).
+struct Problem {
+    const void *in;
+    void *out;
+    int esize;                 // 4 (fp32 bits) or 2 (bf16 bits)
+    int64_t batch, rows, cols;
+    int64_t ld_in, ld_out;
+    int64_t stride_in, stride_out;
+    cudaStream_t stream;
+};
+
+struct TmaConfig {
+    int ctas_per_sm;   // 0 = as many as fit
+    int stages;        // input pipeline depth, 0 = default
+    int tile_order;    // 0 row-major, 1 diagonal
+};
+
+// True when the side's base pointer, row pitch and (for batch > 1) plane pitch
+// are all multiples of 16 bytes, so 16-byte vector or TMA accesses are legal.
+inline bool side_aligned16(const void *base, int64_t ld, int64_t stride, int64_t batch,
+                           int esize) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return false;
+    if ((ld * esize) & 15) return false;
+    if (batch > 1 && ((stride * esize) & 15)) return false;
+    return true;
+}
+
+// Launchers: each returns the CUDA error of the launch (cudaSuccess when fine).
+cudaError_t launch_naive(const Problem &p, bool read_coalesced);
+cudaError_t launch_tile_pad(const Problem &p, int pad);
+cudaError_t launch_tile_vec(const Problem &p, bool vec_in, bool vec_out, int tile_order);
+// TMA path: may fail in tensor-map encoding (driver error) as well as launch.
+// `why` receives a static message for non-CUDA failures.
+cudaError_t launch_tma(const Problem &p, const TmaConfig &cfg, const char **why);
+cudaError_t launch_copy(const void *in, void *out, size_t bytes, cudaStream_t stream);
+
+// Device-side fault flag (bounded waits that ran out).  Reads and clears it.
+cudaError_t read_and_clear_fault(unsigned *value);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace tr

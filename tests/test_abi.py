@@ -1,0 +1,153 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments before any CUDA call (no GPU needed)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from shared_memory_tiled_gb300 import binding as B
+from shared_memory_tiled_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "transpose.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["tr_transpose_f32", "tr_transpose_bf16", "tr_transpose_batched_f32",
+                     "tr_transpose_batched_bf16", "tr_copy", "tr_transpose_ex",
+                     "tr_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in transpose.h but not exported"
+    assert set(declared_functions()) == set(B.SIGNATURES), "binding and header disagree"
+
+
+def test_exports_are_c_linkage(lib):
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (tr_[a-z0-9_]+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_version_and_strings(lib):
+    assert B.tr_version() == 10000
+    for s in B.Status:
+        msg = B.tr_status_string(s)
+        assert msg and msg != "unknown status"
+    assert B.tr_status_string(99) == "unknown status"
+    assert isinstance(B.tr_last_error(), str)
+
+
+FAKE_IN, FAKE_OUT = 0x7F0000000000, 0x7F1000000000  # never dereferenced
+
+
+@pytest.mark.parametrize("fn", ["tr_transpose_f32", "tr_transpose_bf16"])
+def test_single_matrix_argument_errors(lib, fn):
+    f = getattr(B, fn)
+    assert f(FAKE_IN, FAKE_OUT, -1, 4, 4, 4) == B.Status.ERR_BAD_DIM
+    assert f(FAKE_IN, FAKE_OUT, 4, -1, 4, 4) == B.Status.ERR_BAD_DIM
+    assert f(0, FAKE_OUT, 4, 4, 4, 4) == B.Status.ERR_NULL
+    assert f(FAKE_IN, 0, 4, 4, 4, 4) == B.Status.ERR_NULL
+    assert f(FAKE_IN, FAKE_OUT, 4, 5, 4, 4) == B.Status.ERR_BAD_LD     # ld_in < cols
+    assert f(FAKE_IN, FAKE_OUT, 5, 4, 4, 4) == B.Status.ERR_BAD_LD     # ld_out < rows
+    # overlapping ranges: output starts inside the input extent
+    assert f(FAKE_IN, FAKE_IN + 8, 4, 4, 4, 4) == B.Status.ERR_OVERLAP
+    assert f(FAKE_IN + 8, FAKE_IN, 4, 4, 4, 4) == B.Status.ERR_OVERLAP
+    # overflowing extents
+    assert f(FAKE_IN, FAKE_OUT, 1 << 40, 1 << 40, 1 << 40, 1 << 40) == B.Status.ERR_BAD_DIM
+    # empty problems succeed without touching anything, even with NULL pointers
+    assert f(0, 0, 0, 5, 5, 0) == B.Status.OK
+    assert f(0, 0, 7, 0, 0, 7) == B.Status.OK
+
+
+@pytest.mark.parametrize("fn", ["tr_transpose_batched_f32", "tr_transpose_batched_bf16"])
+def test_batched_argument_errors(lib, fn):
+    f = getattr(B, fn)
+    assert f(FAKE_IN, FAKE_OUT, -1, 4, 4, 4, 4, 16, 16) == B.Status.ERR_BAD_DIM
+    assert f(FAKE_IN, FAKE_OUT, 2, 4, 4, 4, 4, 15, 16) == B.Status.ERR_BAD_LD
+    assert f(FAKE_IN, FAKE_OUT, 2, 4, 4, 4, 4, 16, 15) == B.Status.ERR_BAD_LD
+    # planes may pack tighter than rows*ld when the last row is short (checked
+    # with the planner, which validates without launching)
+    dt = B.DType.F32 if fn.endswith("f32") else B.DType.BF16
+    assert _plan(FAKE_IN, FAKE_OUT, dt, 2, 4, 3, 5, 4, 18, 12) > 0
+    assert _plan(FAKE_IN, FAKE_OUT, dt, 2, 4, 3, 5, 4, 17, 12) == -B.Status.ERR_BAD_LD
+    assert f(0, 0, 0, 4, 4, 4, 4, 16, 16) == B.Status.OK
+    # overlap found through the last plane
+    es = 4 if fn.endswith("f32") else 2
+    assert f(FAKE_IN, FAKE_IN + es * 20, 2, 4, 4, 4, 4, 16, 16) == B.Status.ERR_OVERLAP
+
+
+def test_copy_argument_errors(lib):
+    assert B.tr_copy(0, FAKE_OUT, 16) == B.Status.ERR_NULL
+    assert B.tr_copy(FAKE_IN, FAKE_IN + 8, 16) == B.Status.ERR_OVERLAP
+    assert B.tr_copy(0, 0, 0) == B.Status.OK
+
+
+def _plan(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, si=0, so=0, **opt):
+    a = B.make_args(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, si, so)
+    return B.tr_plan_variant(a, B.make_options(**opt) if opt else None)
+
+
+def test_planner(lib):
+    F32, BF16 = B.DType.F32, B.DType.BF16
+    # 16-byte aligned bases and pitches on both sides -> TMA
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 8192, 8192, 8192, 8192) == B.Variant.TMA
+    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 16384, 16384, 16384, 16384) == B.Variant.TMA
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 64, 2048, 1536, 1536, 2048, 2048 * 1536,
+                 1536 * 2048) == B.Variant.TMA
+    # a 12289-element output pitch is not a multiple of 16 bytes -> LSU vector tile
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 12289, 7919, 7936, 12289) == B.Variant.TILE_VEC
+    # a misaligned base pointer -> LSU vector tile
+    assert _plan(FAKE_IN + 4, FAKE_OUT, F32, 1, 64, 64, 64, 64) == B.Variant.TILE_VEC
+    # bf16 pitch 8 elements = 16 bytes is fine, 4 elements is not
+    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 8, 8, 8, 8) == B.Variant.TMA
+    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 4, 4, 4, 4) == B.Variant.TILE_VEC
+    # batched with a plane pitch that breaks 16-byte alignment -> LSU
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 2, 4, 4, 4, 4, 17, 16) == B.Variant.TILE_VEC
+    # explicit requests are honoured
+    for v in B.Variant:
+        if v != B.Variant.AUTO:
+            assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 64, 64, variant=v) == v
+    # invalid arguments and options come back as negative statuses
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, -1, 4, 4, 4) == -B.Status.ERR_BAD_DIM
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, variant=9) == -B.Status.ERR_UNSUPPORTED
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, stages=1) == -B.Status.ERR_UNSUPPORTED
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, pad=5) == -B.Status.ERR_UNSUPPORTED
+    assert _plan(FAKE_IN, FAKE_OUT, 7, 1, 4, 4, 4, 4) == -B.Status.ERR_UNSUPPORTED
+
+
+def test_ex_rejects_bad_options_and_reserved_fields(lib):
+    a = B.make_args(FAKE_IN, FAKE_OUT, B.DType.F32, 1, 4, 4, 4, 4)
+    assert B.tr_transpose_ex(a, B.make_options(variant=42)) == B.Status.ERR_UNSUPPORTED
+    o = B.make_options()
+    o.reserved[1] = 3
+    assert B.tr_transpose_ex(a, o) == B.Status.ERR_UNSUPPORTED
+    a.reserved = 1
+    assert B.tr_transpose_ex(a, None) == B.Status.ERR_UNSUPPORTED
+    assert B.tr_transpose_ex(B.make_args(0, 0, B.DType.F32, 0, 0, 0, 0, 0)) == B.Status.OK
+    assert B.load().tr_transpose_ex(None, None) == B.Status.ERR_NULL
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(B.LibraryMissing):
+        B.load(str(tmp_path / "nope.so"))
+    monkeypatch.setattr(B, "_lib", None)
