@@ -301,15 +301,16 @@ def run_ours(args):
     # keep the same kernel running for ~1 s more if the timed region was too
     # short for the 100 ms clock samples (the samples then cover this window)
     extra_window = None
-    if t_wall1 - t_wall0 < 1.0:
-        reps = max(1, int(1.0 / max(statistics.median(per_ms) / 1e3, 1e-6)))
+    if t_wall1 - t_wall0 < args.clock_window:
+        reps = max(1, int(args.clock_window / max(statistics.median(per_ms) / 1e3, 1e-6)))
         tw0 = time.time()
         timed(step, reps, 0)
         extra_window = (tw0, time.time())
     sampler.stop()
     clocks = sampler.summary(*(extra_window or (t_wall0, t_wall1)))
     if extra_window:
-        clocks["window"] = "same kernel re-run for 1 s after the timed region"
+        clocks["window"] = (f"timed region shorter than the 100 ms sampling: same kernel "
+                            f"re-run untimed for {args.clock_window:g} s right after it")
 
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
@@ -409,6 +410,9 @@ def main(argv=None):
     ap.add_argument("--tile-order", dest="tile_order", type=int, default=0)
     ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    ap.add_argument("--clock-window", dest="clock_window", type=float, default=1.0,
+                    help="seconds of untimed re-runs for clock sampling when the timed "
+                         "region is shorter than this (0 = none)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # never fewer than 3 untimed warm-up steps
     if args.impl == "reference":
