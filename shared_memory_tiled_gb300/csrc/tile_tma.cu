@@ -34,6 +34,14 @@
 //   a buffer is reusable only after its readers finish).
 // Every mbarrier wait is bounded; a wait that runs out sets the device fault
 // flag, the CTA drains the copies it has in flight and returns.
+//
+// Ragged output rows: when an output row (rows elements) does not end on a
+// 16-byte boundary, a TMA store writes the row's last 16-byte chunk whole and
+// so would overwrite the output's pitch padding.  Tiles of the last tile row
+// then bypass the output buffer: each thread stores its transposed
+// micro-block with bounds-checked element stores.  Input rows need no such
+// care: extra elements a load brings in land in output rows past `cols`, which
+// the store clips (whole lines).
 #include "ptx.cuh"
 #include "tr_internal.h"
 
@@ -53,9 +61,15 @@ constexpr int kOutStages = 2;
 struct TmaGeom {
     int64_t total;        // batch * tiles_r * tiles_c
     int32_t tiles_r, tiles_c;
-    int32_t rows;         // input rows (= output columns) for store clipping
+    int32_t rows, cols;   // input plane (the output plane is cols x rows)
     int32_t in_stages;
     int32_t diagonal;
+    // Output rows whose length (rows elements) is not a whole number of 16-byte
+    // chunks: a TMA store writes its last chunk whole, which would spill into
+    // the row pitch, so the last tile row is written with element stores.
+    int32_t ragged_out;
+    void *out;            // output base, for those element stores
+    int64_t ld_out, stride_out;
 };
 
 template <typename T>
@@ -164,15 +178,40 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
         const uint32_t parity = uint32_t((k / S) & 1);
         const bool ok = ptx::mbar_wait_bounded(full + slot, parity);
 
+        int32_t b, tr, tc;
+        tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
+        const bool direct = g.ragged_out && tr == g.tiles_r - 1;
+
         const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
         uint8_t *ob = out_buf + size_t(k & 1) * L::BUF_BYTES;
         uint4 x[V], y[V];
 #pragma unroll
         for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
         micro_transpose(x, y);
+        if (!direct) {
 #pragma unroll
-        for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[m]) = y[m];
-        ptx::fence_proxy_async_smem();
+            for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[m]) = y[m];
+            ptx::fence_proxy_async_smem();
+        } else if (ok) {
+            // Last tile row of a ragged output: bounds-checked element stores.
+            T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
+            const int64_t oc = int64_t(tr) * L::TILE + V * A;
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                const int64_t orow = int64_t(tc) * L::TILE + V * C + m;
+                if (orow < g.cols) {
+                    const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        if (oc + e < g.rows) {
+                            const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
+                            dst[orow * g.ld_out + oc + e] =
+                                T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
+                        }
+                    }
+                }
+            }
+        }
         // The store issued for tile k-1 must finish reading its buffer before
         // tile k+1 is written there (two output buffers).
         if (t == 0) ptx::bulk_wait_group_read<kOutStages - 2>();
@@ -181,12 +220,13 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
             break;
         }
         if (t == 0) {
-            int32_t b, tr, tc;
-            tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
-            ptx::tma_store_3d(&tm_out, ob, tr * L::TILE, tc * L::TILE, b);
-            if (tr * L::TILE + L::BOXC < g.rows)
-                ptx::tma_store_3d(&tm_out, ob + L::BOX_BYTES, tr * L::TILE + L::BOXC, tc * L::TILE,
-                                  b);
+            if (!direct) {
+                ptx::tma_store_3d(&tm_out, ob, tr * L::TILE, tc * L::TILE, b);
+                if (tr * L::TILE + L::BOXC < g.rows)
+                    ptx::tma_store_3d(&tm_out, ob + L::BOX_BYTES, tr * L::TILE + L::BOXC,
+                                      tc * L::TILE, b);
+            }
+            // An empty group keeps the count of committed groups one per tile.
             ptx::bulk_commit_group();
             if (k + S < n_local) issue_load(k + S, slot);
         }
@@ -271,7 +311,12 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     g.tiles_c = int32_t((p.cols + L::TILE - 1) / L::TILE);
     g.total = p.batch * int64_t(g.tiles_r) * g.tiles_c;
     g.rows = int32_t(p.rows);
+    g.cols = int32_t(p.cols);
     g.diagonal = cfg.tile_order == 1;
+    g.ragged_out = (p.rows * p.esize) % 16 != 0;
+    g.out = p.out;
+    g.ld_out = p.ld_out;
+    g.stride_out = sout;
     int stages = cfg.stages > 0 ? cfg.stages : (sizeof(T) == 4 ? 4 : 3);
     if (stages < 2) stages = 2;
     if (stages > 8) stages = 8;

@@ -51,8 +51,9 @@ def _variants(dtype, aligned):
           dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
           dict(variant=V.TILE_PAD, pad=2), dict(variant=V.TILE_VEC), dict(variant=V.AUTO)]
     if aligned:
-        vs += [dict(variant=V.TMA), dict(variant=V.TMA, stages=2), dict(variant=V.TMA, stages=6,
-                                                                          tile_order=1)]
+        deep = 6 if dtype is U32 else 4   # 8 x 32 KiB bf16 stages would not fit
+        vs += [dict(variant=V.TMA), dict(variant=V.TMA, stages=2),
+               dict(variant=V.TMA, stages=deep, tile_order=1)]
     return vs
 
 
@@ -72,7 +73,11 @@ def test_pitched_and_batched(dtype):
     al = 16 // np.dtype(dtype).itemsize
     for (b, r, c, pi, po, pp) in [(1, 130, 70, al, 2 * al, 0), (3, 65, 129, 3, 5, 7),
                                   (4, 96, 160, al, al, 4 * al), (2, 129, 257, 1, 0, 1),
-                                  (5, 8, 8, 0, 0, 0), (1, 70, 130, 6 * al, 3, 0)]:
+                                  (5, 8, 8, 0, 0, 0), (1, 70, 130, 6 * al, 3, 0),
+                                  # 16-byte aligned pitches but output rows that end
+                                  # mid-chunk (the TMA path's element-store edge)
+                                  (1, 190, 250, 6, 10, 0), (2, 190, 250, 6, 10, 8),
+                                  (1, 61, 64, 0, 3, 0), (3, 129, 8, 0, 7, 0)]:
         x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=b + r + c)
         es = np.dtype(dtype).itemsize
         aligned = all(v * es % 16 == 0 for v in (geo[3], geo[4])) and \
@@ -92,6 +97,13 @@ def test_misaligned_base_pointers(dtype):
         with pytest.raises(B.TransposeError) as e:
             gpu_out(x, prefill, *geo, variant=V.TMA, in_off=in_off, out_off=out_off)
         assert e.value.status == B.Status.ERR_UNSUPPORTED
+
+
+def test_tma_stage_count_that_does_not_fit_is_refused():
+    x, prefill, geo = case(U16, 1, 128, 128)
+    with pytest.raises(B.TransposeError) as e:
+        gpu_out(x, prefill, *geo, variant=V.TMA, stages=8)
+    assert e.value.status == B.Status.ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("dtype", [U32, U16], ids=["f32", "bf16"])
