@@ -53,27 +53,38 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of the sources the timed kernels are built from; a recorded ncu
-    traffic figure is reported only while it still matches."""
+# Source files each kernel is built from (the hash of these decides whether a
+# recorded ncu traffic figure still describes the kernel that runs).
+KERNEL_SOURCES = {
+    "k_tile_vec": ["tile_vec.cu", "tile_geom.cuh", "tr_internal.h"],
+    "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
+    "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
+    "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
+    "k_copy_aligned": ["copy.cu", "tr_internal.h"],
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the sources a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_memory_tiled_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """dram bytes per launch from the committed ncu summary, or None."""
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when there
+    is none or the kernel's sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        rec = d.get(kernel_key)
-        if rec and rec.get("source_hash") == kernel_source_hash():
-            return rec.get("dram_bytes_per_launch"), rec.get("scaled_from")
+        rec = d.get(f"{kernel}:{workload}")
+        if rec and kernel in KERNEL_SOURCES and rec.get("source_hash") == kernel_source_hash(kernel):
+            return rec.get("dram_bytes_per_launch"), rec.get("note")
     except Exception:
         pass
     return None, None
@@ -254,7 +265,9 @@ def run_ours(args):
     targs = B.make_args(d_in.data_ptr(), d_out.data_ptr(), dt, w.batch, w.rows, w.cols, w.ld_in,
                         w.ld_out, w.sin, w.sout, sptr)
     topts = B.make_options(variant, pad=args.pad, stages=args.stages,
-                           ctas_per_sm=args.ctas_per_sm, tile_order=args.tile_order)
+                           ctas_per_sm=args.ctas_per_sm, tile_order=args.tile_order,
+                           out_stages=args.out_stages, tile_rows=args.tile_rows,
+                           tile_cols=args.tile_cols)
     planned = B.Variant(B.tr_plan_variant(targs, topts))
     lib = B.load()
     ex = lib.tr_transpose_ex
@@ -353,7 +366,7 @@ def run_ours(args):
     peak, peak_kind = read_peaks()
     kname = {B.Variant.TMA: "k_tma", B.Variant.TILE_VEC: "k_tile_vec",
              B.Variant.TILE_PAD: "k_tile_pad"}.get(planned, str(planned.name).lower())
-    traffic, traffic_note = recorded_traffic(f"{kname}:{w.name}")
+    traffic, traffic_note = recorded_traffic(kname, w.name)
 
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
@@ -408,6 +421,9 @@ def main(argv=None):
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--ctas-per-sm", dest="ctas_per_sm", type=int, default=0)
     ap.add_argument("--tile-order", dest="tile_order", type=int, default=0)
+    ap.add_argument("--out-stages", dest="out_stages", type=int, default=0)
+    ap.add_argument("--tile-rows", dest="tile_rows", type=int, default=0)
+    ap.add_argument("--tile-cols", dest="tile_cols", type=int, default=0)
     ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
     ap.add_argument("--clock-window", dest="clock_window", type=float, default=1.0,

@@ -93,14 +93,20 @@ typedef enum tr_variant {
     TR_VARIANT_TMA = 5
 } tr_variant;
 
-/* Tuning knobs for tr_transpose_ex.  Zero-initialise for defaults. */
+/* Tuning knobs for tr_transpose_ex.  Zero-initialise for defaults.
+ * TILE_VEC tile shapes (rows x cols, elements): fp32 64x64 (default), 128x64,
+ * 64x128, 128x128; bf16 128x128 (default), 256x128, 128x256.  Other shapes
+ * return TR_ERR_UNSUPPORTED. */
 typedef struct tr_options {
     int32_t variant;      /* tr_variant                                                  */
     int32_t pad;          /* TILE_PAD: shared row pitch is 32 + pad elements, 0..8        */
     int32_t ctas_per_sm;  /* TMA: persistent CTAs per SM, 0 = as many as fit (max 8)      */
     int32_t stages;       /* TMA: input pipeline depth 2..8, 0 = default                  */
     int32_t tile_order;   /* TMA/TILE_VEC: 0 = row-major tile walk, 1 = diagonal          */
-    int32_t reserved[3];  /* must be zero                                                 */
+    int32_t out_stages;   /* TMA: output buffers (stores in flight) 2..4, 0 = default     */
+    int32_t tile_rows;    /* TILE_VEC: tile rows in elements, 0 = default (see below)     */
+    int32_t tile_cols;    /* TILE_VEC: tile columns in elements, 0 = default              */
+    int32_t reserved[2];  /* must be zero                                                 */
 } tr_options;
 
 /* Full argument set of one (possibly batched) transpose; see the conventions

@@ -58,7 +58,9 @@ class Variant(enum.IntEnum):
 class Options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("pad", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("tile_order", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("tile_order", ctypes.c_int32), ("out_stages", ctypes.c_int32),
+                ("tile_rows", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class Args(ctypes.Structure):
@@ -147,8 +149,10 @@ def make_args(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, stride_i
                 stride_out, stream)
 
 
-def make_options(variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0, tile_order=0) -> Options:
-    return Options(int(variant), pad, ctas_per_sm, stages, tile_order, (ctypes.c_int32 * 3)())
+def make_options(variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0, tile_order=0,
+                 out_stages=0, tile_rows=0, tile_cols=0) -> Options:
+    return Options(int(variant), pad, ctas_per_sm, stages, tile_order, out_stages, tile_rows,
+                   tile_cols, (ctypes.c_int32 * 2)())
 
 
 def tr_transpose_ex(args: Args, opts: Options | None = None) -> int:
@@ -215,7 +219,7 @@ def _geometry(t):
 
 
 def transpose(x, out=None, *, variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0,
-              tile_order=0, stream=None):
+              tile_order=0, out_stages=0, tile_rows=0, tile_cols=0, stream=None):
     """Transpose the last two dims of a CUDA tensor ``x`` ([R, C] or [B, R, C]).
 
     ``out`` (optional) receives the result and may be a strided view (its row
@@ -239,7 +243,8 @@ def transpose(x, out=None, *, variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages
         stream = torch.cuda.current_stream(x.device).cuda_stream
     args = make_args(x.data_ptr(), out.data_ptr(), dt, b, r, c, ld_in, ld_out, s_in, s_out,
                      stream)
-    opts = make_options(variant, pad, ctas_per_sm, stages, tile_order)
+    opts = make_options(variant, pad, ctas_per_sm, stages, tile_order, out_stages, tile_rows,
+                        tile_cols)
     check(tr_transpose_ex(args, opts))
     return out
 

@@ -93,21 +93,39 @@ bool options_valid(const tr_options *o) {
     if (o->ctas_per_sm < 0 || o->ctas_per_sm > 8) return false;
     if (o->stages != 0 && (o->stages < 2 || o->stages > 8)) return false;
     if (o->tile_order < 0 || o->tile_order > 1) return false;
+    if (o->out_stages != 0 && (o->out_stages < 2 || o->out_stages > 4)) return false;
+    if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
+        return false;
     for (int r : o->reserved)
         if (r != 0) return false;
     return true;
 }
 
-// Variant choice (host logic only).  AUTO takes TMA when both sides allow
-// 16-byte aligned tiles, else the vectorised LSU tile, which itself falls back
-// to single-element global accesses on a misaligned side.
+// Variant choice (host logic only).  AUTO takes the vectorised swizzled tile,
+// the fastest variant measured on GB300 for every alignment class: it uses
+// 16-byte accesses on each side that allows them, realigns misaligned output
+// rows with warp shuffles, and loads single elements from a misaligned input.
+// TMA runs only when asked for.
 int32_t choose(const Problem &p, const tr_options *o) {
+    (void)p;
     const int req = o ? o->variant : TR_VARIANT_AUTO;
     if (req != TR_VARIANT_AUTO) return req;
-    const bool in16 = side_aligned16(p.in, p.ld_in, p.stride_in, p.batch, p.esize);
-    const bool out16 = side_aligned16(p.out, p.ld_out, p.stride_out, p.batch, p.esize);
-    if (in16 && out16) return TR_VARIANT_TMA;
     return TR_VARIANT_TILE_VEC;
+}
+
+// Tile shape AUTO uses for the vectorised tile.  Output rows that are not
+// 16-byte aligned pay a few single-element stores at both ends of every row
+// segment, so they take tiles twice as tall (longer output segments).
+void auto_vec_shape(const Problem &p, bool out16, int *rows, int *cols) {
+    if (out16) {
+        *rows = *cols = 0;  // kernel default: 64x64 fp32, 128x128 bf16
+    } else if (p.esize == 4) {
+        *rows = 128;
+        *cols = 64;
+    } else {
+        *rows = 256;
+        *cols = 128;
+    }
 }
 
 tr_status run(const tr_args *a, const tr_options *o) {
@@ -124,14 +142,26 @@ tr_status run(const tr_args *a, const tr_options *o) {
         case TR_VARIANT_NAIVE_ROW: e = launch_naive(p, true); break;
         case TR_VARIANT_NAIVE_COL: e = launch_naive(p, false); break;
         case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
-        case TR_VARIANT_TILE_VEC: e = launch_tile_vec(p, in16, out16, o ? o->tile_order : 0); break;
+        case TR_VARIANT_TILE_VEC: {
+            VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0};
+            if (cfg.tile_rows == 0 && cfg.tile_cols == 0)
+                auto_vec_shape(p, out16, &cfg.tile_rows, &cfg.tile_cols);
+            const char *why = nullptr;
+            e = launch_tile_vec(p, in16, out16, cfg, &why);
+            if (e != cudaSuccess && why) {
+                set_error(why, cudaSuccess);
+                return TR_ERR_UNSUPPORTED;
+            }
+            break;
+        }
         case TR_VARIANT_TMA: {
             if (!in16 || !out16) {
                 set_error("TMA needs 16-byte aligned base pointers and pitches on both sides",
                           cudaSuccess);
                 return TR_ERR_UNSUPPORTED;
             }
-            TmaConfig cfg{o ? o->ctas_per_sm : 0, o ? o->stages : 0, o ? o->tile_order : 0};
+            TmaConfig cfg{o ? o->ctas_per_sm : 0, o ? o->stages : 0, o ? o->tile_order : 0,
+                          o ? o->out_stages : 0};
             const char *why = nullptr;
             e = launch_tma(p, cfg, &why);
             if (e != cudaSuccess && why) {
@@ -139,7 +169,8 @@ tr_status run(const tr_args *a, const tr_options *o) {
                 if (auto_mode) {
                     // The planner's first choice could not be encoded (e.g. a
                     // plane pitch the tensor map rejects): take the LSU tile.
-                    e = launch_tile_vec(p, in16, out16, cfg.tile_order);
+                    const VecConfig vc{cfg.tile_order, 0, 0};
+                    e = launch_tile_vec(p, in16, out16, vc, &why);
                     break;
                 }
                 set_error(why, cudaSuccess);

@@ -56,13 +56,14 @@ __device__ unsigned g_fault_flag = 0;
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kOutStages = 2;
+constexpr int kMaxOutStages = 4;
 
 struct TmaGeom {
     int64_t total;        // batch * tiles_r * tiles_c
     int32_t tiles_r, tiles_c;
     int32_t rows, cols;   // input plane (the output plane is cols x rows)
-    int32_t in_stages;
+    int32_t in_stages;    // input slots (tile loads in flight)
+    int32_t out_stages;   // output buffers (tile stores in flight), 2..4
     int32_t diagonal;
     // Output rows whose length (rows elements) is not a whole number of 16-byte
     // chunks: a TMA store writes its last chunk whole, which would spill into
@@ -132,7 +133,7 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *in_buf = base;
     uint8_t *out_buf = base + size_t(g.in_stages) * L::BUF_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(out_buf + kOutStages * L::BUF_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_buf + size_t(g.out_stages) * L::BUF_BYTES);
 
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int quad = w >> 1;                      // which 8x8 group of micro-blocks
@@ -150,6 +151,7 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
     const int64_t n_local =
         blockIdx.x < g.total ? (g.total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int S = g.in_stages;
+    const int SO = g.out_stages;
 
     auto issue_load = [&](int64_t k, int slot) {
         int32_t b, tr, tc;
@@ -183,7 +185,7 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
         const bool direct = g.ragged_out && tr == g.tiles_r - 1;
 
         const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
-        uint8_t *ob = out_buf + size_t(k & 1) * L::BUF_BYTES;
+        uint8_t *ob = out_buf + size_t(k % SO) * L::BUF_BYTES;
         uint4 x[V], y[V];
 #pragma unroll
         for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
@@ -212,9 +214,14 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
                 }
             }
         }
-        // The store issued for tile k-1 must finish reading its buffer before
-        // tile k+1 is written there (two output buffers).
-        if (t == 0) ptx::bulk_wait_group_read<kOutStages - 2>();
+        // Tile k+1 goes to the buffer of the store issued for tile k+1-SO: that
+        // store must have finished reading it, so at most SO-2 of the stores
+        // committed so far (tiles .. k-1) may still be reading.
+        if (t == 0) {
+            if (SO == 2) ptx::bulk_wait_group_read<0>();
+            else if (SO == 3) ptx::bulk_wait_group_read<1>();
+            else ptx::bulk_wait_group_read<2>();
+        }
         if (__syncthreads_or(!ok)) {
             aborted = true;
             break;
@@ -281,6 +288,80 @@ bool encode_3d(CUtensorMap *map, const void *base, int esize, int64_t elems, int
     return r == CUDA_SUCCESS;
 }
 
+// Per-device facts and per-configuration occupancy, computed once: the
+// launch path then makes no attribute or occupancy query per call.
+struct DeviceInfo {
+    bool ok = false;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    int max_smem_optin = 0;
+    int fit[2][9][kMaxOutStages + 1] = {};  // [esize==4][in_stages][out_stages], 0 = unknown
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+DeviceInfo &device_info() {
+    static thread_local DeviceInfo failed;
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess || d < 0 || d >= kMaxDevices) {
+        failed.ok = false;
+        failed.err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return failed;
+    }
+    DeviceInfo &info = g_dev[d];
+    if (!info.ok) {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!info.ok) {
+            int sms = 0, optin = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+            // Opt both kernels in to the largest dynamic shared memory once.
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_tma<uint32_t>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_tma<uint16_t>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e != cudaSuccess) {
+                failed.ok = false;
+                failed.err = e;
+                return failed;
+            }
+            info.sms = sms;
+            info.max_smem_optin = optin;
+            info.ok = true;
+        }
+    }
+    return info;
+}
+
+template <typename T>
+size_t smem_bytes(int in_stages, int out_stages) {
+    // 1 KiB of slack to align the buffers to the 128-byte swizzle's 1 KiB
+    // pattern, then the tiles, then one 8-byte mbarrier per input slot.
+    return 1024 + size_t(in_stages + out_stages) * TmaTile<T>::BUF_BYTES + size_t(in_stages) * 8;
+}
+
+template <typename T>
+int resident_ctas(DeviceInfo &dev, int in_stages, int out_stages) {
+    int &slot = dev.fit[sizeof(T) == 4][in_stages][out_stages];
+    if (slot == 0) {
+        int fit = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &fit, k_tma<T>, kThreads, smem_bytes<T>(in_stages, out_stages)) != cudaSuccess)
+            fit = -1;
+        slot = fit < 1 ? -1 : fit;
+    }
+    return slot;
+}
+
+int default_in_stages(size_t esize) { return esize == 4 ? 2 : 2; }
+int default_out_stages(size_t esize) { return esize == 4 ? 2 : 2; }
+
 template <typename T>
 cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **why) {
     using L = TmaTile<T>;
@@ -317,34 +398,29 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     g.out = p.out;
     g.ld_out = p.ld_out;
     g.stride_out = sout;
-    int stages = cfg.stages > 0 ? cfg.stages : (sizeof(T) == 4 ? 4 : 3);
-    if (stages < 2) stages = 2;
-    if (stages > 8) stages = 8;
+    DeviceInfo &dev = device_info();
+    if (!dev.ok) return dev.err;
+    int stages = cfg.stages > 0 ? cfg.stages : default_in_stages(sizeof(T));
+    int out_stages = cfg.out_stages > 0 ? cfg.out_stages : default_out_stages(sizeof(T));
+    if (stages < 2 || stages > 8 || out_stages < 2 || out_stages > kMaxOutStages) {
+        *why = "TMA stage counts out of range";
+        return cudaErrorInvalidValue;
+    }
     g.in_stages = stages;
-    const size_t smem = 1024 + size_t(stages + kOutStages) * L::BUF_BYTES + size_t(stages) * 8;
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int max_optin = 0;
-    e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    if (smem > size_t(max_optin)) {
+    g.out_stages = out_stages;
+    const size_t smem = smem_bytes<T>(stages, out_stages);
+    if (smem > size_t(dev.max_smem_optin)) {
         *why = "TMA pipeline does not fit in shared memory; lower the stage count";
         return cudaErrorInvalidValue;
     }
-    e = cudaFuncSetAttribute(k_tma<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    int fit = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma<T>, kThreads, smem);
-    if (e != cudaSuccess) return e;
+    const int fit = resident_ctas<T>(dev, stages, out_stages);
     if (fit < 1) {
         *why = "TMA kernel cannot be resident with this configuration";
         return cudaErrorInvalidValue;
     }
     int per_sm = cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : fit;
     if (per_sm > fit) per_sm = fit;
-    int64_t grid = int64_t(sm_count()) * per_sm;
+    int64_t grid = int64_t(dev.sms) * per_sm;
     if (grid > g.total) grid = g.total;
     k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
     return cudaGetLastError();

@@ -23,6 +23,7 @@ struct TmaConfig {
     int ctas_per_sm;   // 0 = as many as fit
     int stages;        // input pipeline depth, 0 = default
     int tile_order;    // 0 row-major, 1 diagonal
+    int out_stages;    // output buffers, 0 = default
 };
 
 // True when the side's base pointer, row pitch and (for batch > 1) plane pitch
@@ -35,10 +36,18 @@ inline bool side_aligned16(const void *base, int64_t ld, int64_t stride, int64_t
     return true;
 }
 
+struct VecConfig {
+    int tile_order;    // 0 row-major, 1 diagonal
+    int tile_rows;     // tile shape in elements, 0 = default
+    int tile_cols;
+};
+
 // Launchers: each returns the CUDA error of the launch (cudaSuccess when fine).
 cudaError_t launch_naive(const Problem &p, bool read_coalesced);
 cudaError_t launch_tile_pad(const Problem &p, int pad);
-cudaError_t launch_tile_vec(const Problem &p, bool vec_in, bool vec_out, int tile_order);
+// `why` receives a static message when the configuration itself is refused.
+cudaError_t launch_tile_vec(const Problem &p, bool vec_in, bool vec_out, const VecConfig &cfg,
+                            const char **why);
 // TMA path: may fail in tensor-map encoding (driver error) as well as launch.
 // `why` receives a static message for non-CUDA failures.
 cudaError_t launch_tma(const Problem &p, const TmaConfig &cfg, const char **why);

@@ -1,0 +1,134 @@
+"""Host-side model of shared-memory banking, and the address each lane of a warp
+produces in every shared-memory access of the transpose kernels.
+
+Bank model ("Shared memory and the bank conflict", section "Banks";
+"Shared-memory tiling and bank conflicts", "Calculate the bank mapping"): 32
+banks, successive 4-byte words in successive banks, so word w lives in bank
+w mod 32.  Lanes reading the same word are served together (broadcast,
+"Shared Memory and Bank Conflicts", "how banking works"); different words in
+one bank are served one after another, so an n-way conflict costs n passes.
+
+Accesses wider than 4 bytes are served in phases: a 16-byte access by a warp
+is served 8 lanes at a time (each lane covers 4 consecutive banks), so the
+minimum is 4 passes per warp instruction.  The model counts passes the same
+way: per phase, the largest number of distinct words any bank must deliver.
+
+The per-kernel address functions restate the index arithmetic of the CUDA
+kernels so their conflict degree can be computed here, on the CPU, and then
+compared with the counters Nsight Compute reports on the GPU.
+"""
+from __future__ import annotations
+
+from collections import defaultdict
+
+BANKS = 32
+WORD = 4
+
+
+def passes(byte_addrs, width=4):
+    """Shared-memory passes for one warp instruction in which lane i accesses
+    ``width`` bytes at ``byte_addrs[i]`` (None = inactive lane)."""
+    lanes_per_phase = {4: 32, 8: 16, 16: 8}[width]
+    total = 0
+    for p0 in range(0, 32, lanes_per_phase):
+        words_in_bank = defaultdict(set)
+        for a in byte_addrs[p0:p0 + lanes_per_phase]:
+            if a is None:
+                continue
+            for w in range(a // WORD, (a + width) // WORD):
+                words_in_bank[w % BANKS].add(w)
+        total += max((len(s) for s in words_in_bank.values()), default=0)
+    return total
+
+
+def conflict_degree(byte_addrs, width=4):
+    """Passes divided by the conflict-free minimum (1 = conflict-free)."""
+    minimum = {4: 1, 8: 2, 16: 4}[width]
+    return passes(byte_addrs, width) / minimum
+
+
+# --- the page's 32 x (32+pad) tile, 4-byte elements -------------------------------------
+
+def pad_tile_column_read(pad, col=0, esize=4):
+    """Phase-2 read of the padded tile: lane t reads tile[t][col]."""
+    return [(t * (32 + pad) + col) * esize for t in range(32)]
+
+
+def pad_tile_row_write(pad, row=0, esize=4):
+    """Phase-1 write: lane t writes tile[row][t]."""
+    return [(row * (32 + pad) + t) * esize for t in range(32)]
+
+
+# --- the vectorised swizzled tile (tile_vec.cu) ------------------------------------------
+
+def vec_tile_load_store(warp, k, V=4, MC=16):
+    """Phase-1 16-byte store of load k: thread t holds chunk t % MC of tile row
+    t // MC + k * 256 // MC, stored at chunk position cc ^ ((r // V) % 8)."""
+    out = []
+    for lane in range(32):
+        t = warp * 32 + lane
+        cc, r = t % MC, t // MC + k * (256 // MC)
+        out.append((r * MC + (cc ^ ((r // V) & 7))) * 16)
+    return out
+
+
+def vec_tile_read(warp, m, V=4, MR=16, MC=16, j=0):
+    """Phase-2 16-byte read m of micro-block u = t + 256 j: A = u % MR, C = u // MR,
+    tile row V*A + m, chunk C at position C ^ (A % 8)."""
+    out = []
+    for lane in range(32):
+        u = warp * 32 + lane + 256 * j
+        A, C = u % MR, u // MR
+        out.append(((V * A + m) * MC + (C ^ (A & 7))) * 16)
+    return out
+
+
+# --- the TMA tile with the 128-byte hardware swizzle (tile_tma.cu) ------------------------
+
+def _tma_lane(warp, lane):
+    quad = warp >> 1
+    s = (lane >> 3) + 4 * (warp & 1)
+    c = lane & 7
+    a = c ^ s
+    return 8 * (quad >> 1) + a, 8 * (quad & 1) + c, a, c
+
+
+def tma_read(warp, m, V=4):
+    """LSU read m of the TMA input box: row V*A+m, chunk c at c ^ (row % 8)."""
+    box = 16 * V * 128
+    out = []
+    for lane in range(32):
+        A, C, a, c = _tma_lane(warp, lane)
+        r = V * A + m
+        out.append((C >> 3) * box + r * 128 + ((c ^ (r & 7)) << 4))
+    return out
+
+
+def tma_write(warp, m, V=4):
+    """LSU write m into the TMA output box: row V*C+m, chunk a at a ^ (row % 8)."""
+    box = 16 * V * 128
+    out = []
+    for lane in range(32):
+        A, C, a, c = _tma_lane(warp, lane)
+        o = V * C + m
+        out.append((A >> 3) * box + o * 128 + ((a ^ (o & 7)) << 4))
+    return out
+
+
+# --- the transposed operand store of the padded SGEMM page --------------------------------
+
+def sgemm_as_store(BK, a_stride, j, offset=0):
+    """Lane t of the first warp stores element j of its float4 of A, transposed:
+    innerRowA = t // (BK/4), innerColA = t % (BK/4), word
+    (innerColA*4 + j) * a_stride + innerRowA + offset ("Padded Shared Memory:
+    Eliminating Bank Conflicts", section "How Shared Memory Is Addressed")."""
+    out = []
+    for t in range(32):
+        row, col = t // (BK // 4), t % (BK // 4)
+        out.append(((col * 4 + j) * a_stride + row + offset) * WORD)
+    return out
+
+
+def a_stride(BM, BK):
+    """The page's padding rule: BM + (32 / BK) % 8 ("The Fix Is One Constant")."""
+    return BM + (32 // BK) % 8

@@ -108,20 +108,16 @@ def _plan(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, si=0, so=0, 
 
 def test_planner(lib):
     F32, BF16 = B.DType.F32, B.DType.BF16
-    # 16-byte aligned bases and pitches on both sides -> TMA
-    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 8192, 8192, 8192, 8192) == B.Variant.TMA
-    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 16384, 16384, 16384, 16384) == B.Variant.TMA
-    assert _plan(FAKE_IN, FAKE_OUT, F32, 64, 2048, 1536, 1536, 2048, 2048 * 1536,
-                 1536 * 2048) == B.Variant.TMA
-    # a 12289-element output pitch is not a multiple of 16 bytes -> LSU vector tile
-    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 12289, 7919, 7936, 12289) == B.Variant.TILE_VEC
-    # a misaligned base pointer -> LSU vector tile
-    assert _plan(FAKE_IN + 4, FAKE_OUT, F32, 1, 64, 64, 64, 64) == B.Variant.TILE_VEC
-    # bf16 pitch 8 elements = 16 bytes is fine, 4 elements is not
-    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 8, 8, 8, 8) == B.Variant.TMA
-    assert _plan(FAKE_IN, FAKE_OUT, BF16, 1, 4, 4, 4, 4) == B.Variant.TILE_VEC
-    # batched with a plane pitch that breaks 16-byte alignment -> LSU
-    assert _plan(FAKE_IN, FAKE_OUT, F32, 2, 4, 4, 4, 4, 17, 16) == B.Variant.TILE_VEC
+    # AUTO takes the vectorised swizzled tile for every alignment class
+    # (aligned, misaligned output pitch, misaligned base, batched)
+    for case in [(FAKE_IN, FAKE_OUT, F32, 1, 8192, 8192, 8192, 8192),
+                 (FAKE_IN, FAKE_OUT, BF16, 1, 16384, 16384, 16384, 16384),
+                 (FAKE_IN, FAKE_OUT, F32, 64, 2048, 1536, 1536, 2048, 2048 * 1536, 1536 * 2048),
+                 (FAKE_IN, FAKE_OUT, F32, 1, 12289, 7919, 7936, 12289),
+                 (FAKE_IN + 4, FAKE_OUT, F32, 1, 64, 64, 64, 64),
+                 (FAKE_IN, FAKE_OUT, BF16, 1, 4, 4, 4, 4),
+                 (FAKE_IN, FAKE_OUT, F32, 2, 4, 4, 4, 4, 17, 16)]:
+        assert _plan(*case) == B.Variant.TILE_VEC
     # explicit requests are honoured
     for v in B.Variant:
         if v != B.Variant.AUTO:

@@ -46,13 +46,18 @@ SHAPES = [(1, 1), (1, 300), (300, 1), (64, 64), (128, 128), (200, 333), (257, 12
           (1000, 77), (33, 1031)]
 
 
+VEC_SHAPES = {U32: [(128, 64), (64, 128), (128, 128)], U16: [(256, 128), (128, 256)]}
+
+
 def _variants(dtype, aligned):
     vs = [dict(variant=V.NAIVE_ROW), dict(variant=V.NAIVE_COL),
           dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
           dict(variant=V.TILE_PAD, pad=2), dict(variant=V.TILE_VEC), dict(variant=V.AUTO)]
+    vs += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]]
     if aligned:
         deep = 6 if dtype is U32 else 4   # 8 x 32 KiB bf16 stages would not fit
-        vs += [dict(variant=V.TMA), dict(variant=V.TMA, stages=2),
+        vs += [dict(variant=V.TMA), dict(variant=V.TMA, stages=3, out_stages=3),
+               dict(variant=V.TMA, stages=2, out_stages=4, ctas_per_sm=1),
                dict(variant=V.TMA, stages=deep, tile_order=1)]
     return vs
 
@@ -91,12 +96,32 @@ def test_misaligned_base_pointers(dtype):
     """Base pointers off a 16-byte boundary: the vector tile falls back to
     single-element accesses on that side; TMA refuses."""
     x, prefill, geo = case(dtype, 2, 100, 136, 8, 8, seed=3)
-    for in_off, out_off in [(1, 0), (0, 1), (3, 5)]:
-        for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC), dict(variant=V.TILE_PAD, pad=1)]:
+    for in_off, out_off in [(1, 0), (0, 1), (3, 5), (2, 7)]:
+        for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC), dict(variant=V.TILE_PAD, pad=1)] + \
+                [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]]:
             check(x, prefill, geo, in_off=in_off, out_off=out_off, **kw)
         with pytest.raises(B.TransposeError) as e:
             gpu_out(x, prefill, *geo, variant=V.TMA, in_off=in_off, out_off=out_off)
         assert e.value.status == B.Status.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", [U32, U16], ids=["f32", "bf16"])
+def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
+    """Odd output pitches: every output row starts at a different offset from a
+    16-byte boundary (the shifted-store path), full tiles and ragged edges."""
+    for (b, r, c, pi, po, pp) in [(1, 515, 300, 4, 1, 0), (2, 256, 256, 0, 3, 5),
+                                  (1, 1025, 263, 9, 0, 0), (3, 130, 129, 7, 2, 1)]:
+        x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=r + c)
+        for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC)] + \
+                [dict(variant=V.TILE_VEC, tile_rows=rr, tile_cols=cc) for rr, cc in VEC_SHAPES[dtype]]:
+            check(x, prefill, geo, **kw)
+
+
+def test_unsupported_vector_tile_shape_is_refused():
+    x, prefill, geo = case(U32, 1, 64, 64)
+    with pytest.raises(B.TransposeError) as e:
+        gpu_out(x, prefill, *geo, variant=V.TILE_VEC, tile_rows=96, tile_cols=64)
+    assert e.value.status == B.Status.ERR_UNSUPPORTED
 
 
 def test_tma_stage_count_that_does_not_fit_is_refused():
@@ -160,6 +185,8 @@ def test_workload_full_size(name):
     es = w.esize
     aligned = (w.ld_in * es % 16 == 0 and w.ld_out * es % 16 == 0)
     kws = [dict(variant=V.AUTO), dict(variant=V.TILE_VEC)]
+    kws += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c)
+            for r, c in VEC_SHAPES[U32 if es == 4 else U16]]
     if aligned:
         kws.append(dict(variant=V.TMA))
     if name.startswith("c1"):
