@@ -106,7 +106,12 @@ typedef struct tr_options {
     int32_t out_stages;   /* TMA: output buffers (stores in flight) 2..4, 0 = default     */
     int32_t tile_rows;    /* TILE_VEC: tile rows in elements, 0 = default (see below)     */
     int32_t tile_cols;    /* TILE_VEC: tile columns in elements, 0 = default              */
-    int32_t reserved[2];  /* must be zero                                                 */
+    int32_t schedule;     /* TILE_VEC: 0 = default, 1 = one tile per block,
+                           *   2 = persistent blocks that prefetch their next tile;
+                           * TMA: 0 = default, 1 = one pipeline per block (64x64 fp32 /
+                           *   128x128 bf16 tiles, one block barrier per tile),
+                           *   2 = one pipeline per warp (32x32 fp32 / 64x64 bf16 tiles) */
+    int32_t reserved[1];  /* must be zero                                                 */
 } tr_options;
 
 /* Full argument set of one (possibly batched) transpose; see the conventions

@@ -96,6 +96,7 @@ bool options_valid(const tr_options *o) {
     if (o->out_stages != 0 && (o->out_stages < 2 || o->out_stages > 4)) return false;
     if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
         return false;
+    if (o->schedule < 0 || o->schedule > 2) return false;
     for (int r : o->reserved)
         if (r != 0) return false;
     return true;
@@ -143,7 +144,8 @@ tr_status run(const tr_args *a, const tr_options *o) {
         case TR_VARIANT_NAIVE_COL: e = launch_naive(p, false); break;
         case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
         case TR_VARIANT_TILE_VEC: {
-            VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0};
+            VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
+                          o && o->schedule == 2};
             if (cfg.tile_rows == 0 && cfg.tile_cols == 0)
                 auto_vec_shape(p, out16, &cfg.tile_rows, &cfg.tile_cols);
             const char *why = nullptr;
@@ -161,7 +163,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
                 return TR_ERR_UNSUPPORTED;
             }
             TmaConfig cfg{o ? o->ctas_per_sm : 0, o ? o->stages : 0, o ? o->tile_order : 0,
-                          o ? o->out_stages : 0};
+                          o ? o->out_stages : 0, o ? o->schedule : 0};
             const char *why = nullptr;
             e = launch_tma(p, cfg, &why);
             if (e != cudaSuccess && why) {
@@ -169,7 +171,8 @@ tr_status run(const tr_args *a, const tr_options *o) {
                 if (auto_mode) {
                     // The planner's first choice could not be encoded (e.g. a
                     // plane pitch the tensor map rejects): take the LSU tile.
-                    const VecConfig vc{cfg.tile_order, 0, 0};
+                    VecConfig vc{cfg.tile_order, 0, 0, false};
+                    auto_vec_shape(p, out16, &vc.tile_rows, &vc.tile_cols);
                     e = launch_tile_vec(p, in16, out16, vc, &why);
                     break;
                 }

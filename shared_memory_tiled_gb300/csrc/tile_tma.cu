@@ -251,6 +251,147 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
     }
 }
 
+// ---------------------------------------------------------------------------
+// Per-warp pipelines.  The CTA-wide pipeline above stalls every warp on one
+// barrier per tile and leaves the loads to one thread of the block.  Here each
+// warp is its own pipeline over its own tiles (warp w of the grid takes tiles
+// w, w + warps, ...): lane 0 keeps `in_stages` TMA box loads in flight on the
+// warp's mbarriers, the 32 lanes turn each tile around and lane 0 stores it
+// with one TMA box store.  The only synchronisation is __syncwarp, so warps
+// and blocks never wait for one another.
+//
+// Tile: one 128-byte-wide box each way, 8V x 8V elements (32x32 fp32, 64x64
+// bf16), 8 x 8 micro-blocks; each lane owns two, (a, c) = (x ^ s, x) with
+// x = lane % 8 and s = lane / 8 + 4p for p = 0, 1, so every 8-lane phase of a
+// 16-byte shared access hits 8 distinct positions (see the analysis above).
+template <typename T>
+struct WarpTile {
+    static constexpr int V = 16 / int(sizeof(T));
+    static constexpr int TILE = 8 * V;        // elements per tile side
+    static constexpr int BYTES = TILE * 128;  // one box: 4 KiB fp32, 8 KiB bf16
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
+           TmaGeom g) {
+    using L = WarpTile<T>;
+    constexpr int V = L::V;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int S = g.in_stages, SO = g.out_stages;
+    const size_t per_warp = size_t(S + SO) * L::BYTES;
+    uint8_t *in_buf = base + warp * per_warp;
+    uint8_t *out_buf = in_buf + size_t(S) * L::BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + nwarps * per_warp) + warp * S;
+
+    const int x = lane & 7;
+    int aa[2];
+    uint32_t roff[2][V], woff[2][V];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int s = (lane >> 3) + 4 * p, a = x ^ s;
+        aa[p] = a;
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+            const int r = V * a + m, o = V * x + m;
+            roff[p][m] = r * 128 + ((x ^ (r & 7)) << 4);
+            woff[p][m] = o * 128 + ((a ^ (o & 7)) << 4);
+        }
+    }
+
+    const int64_t gw = int64_t(blockIdx.x) * nwarps + warp;
+    const int64_t G = int64_t(gridDim.x) * nwarps;
+    const int64_t n_local = gw < g.total ? (g.total - 1 - gw) / G + 1 : 0;
+
+    auto issue_load = [&](int64_t k, int slot) {
+        int32_t b, tr, tc;
+        tile_coords(g, gw + k * G, b, tr, tc);
+        ptx::mbar_arrive_expect_tx(full + slot, L::BYTES);
+        ptx::tma_load_3d(in_buf + size_t(slot) * L::BYTES, &tm_in, full + slot, tc * L::TILE,
+                         tr * L::TILE, b);
+    };
+
+    if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_in);
+        ptx::prefetch_tensormap(&tm_out);
+        for (int i = 0; i < S; ++i) ptx::mbar_init(full + i, 1);
+        ptx::fence_barrier_init();
+        for (int64_t k = 0; k < n_local && k < S; ++k) issue_load(k, int(k));
+    }
+    __syncwarp();
+
+    int64_t k = 0;
+    bool aborted = false;
+    for (; k < n_local; ++k) {
+        const int slot = int(k % S);
+        const bool ok = ptx::mbar_wait_bounded(full + slot, uint32_t((k / S) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            aborted = true;
+            break;
+        }
+        int32_t b, tr, tc;
+        tile_coords(g, gw + k * G, b, tr, tc);
+        const bool direct = g.ragged_out && tr == g.tiles_r - 1;
+        const uint8_t *ib = in_buf + size_t(slot) * L::BYTES;
+        uint8_t *ob = out_buf + size_t(k % SO) * L::BYTES;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint4 xv[V], yv[V];
+#pragma unroll
+            for (int m = 0; m < V; ++m) xv[m] = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
+            micro_transpose(xv, yv);
+            if (!direct) {
+#pragma unroll
+                for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[p][m]) = yv[m];
+            } else {
+                // Last tile row of a ragged output: bounds-checked element stores.
+                T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
+                const int64_t oc = int64_t(tr) * L::TILE + V * aa[p];
+#pragma unroll
+                for (int m = 0; m < V; ++m) {
+                    const int64_t orow = int64_t(tc) * L::TILE + V * x + m;
+                    if (orow < g.cols) {
+                        const uint32_t wv[4] = {yv[m].x, yv[m].y, yv[m].z, yv[m].w};
+#pragma unroll
+                        for (int e = 0; e < V; ++e) {
+                            if (oc + e < g.rows) {
+                                const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
+                                dst[orow * g.ld_out + oc + e] =
+                                    T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!direct) ptx::fence_proxy_async_smem();
+        if (lane == 0) {
+            // The next tile's output buffer was last read by the store issued
+            // SO-1 tiles ago: at most SO-2 stores may still be reading.
+            if (SO == 2) ptx::bulk_wait_group_read<0>();
+            else if (SO == 3) ptx::bulk_wait_group_read<1>();
+            else ptx::bulk_wait_group_read<2>();
+        }
+        __syncwarp();
+        if (lane == 0) {
+            if (!direct) ptx::tma_store_3d(&tm_out, ob, tr * L::TILE, tc * L::TILE, b);
+            ptx::bulk_commit_group();
+            if (k + S < n_local) issue_load(k + S, slot);
+        }
+    }
+    if (lane == 0) {
+        if (aborted) {
+            atomicExch(&g_fault_flag, 1u);
+            for (int64_t kk = k; kk < n_local && kk < k + S; ++kk)
+                ptx::mbar_wait_bounded(full + int(kk % S), uint32_t((kk / S) & 1));
+        }
+        ptx::bulk_wait_group<0>();
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -295,10 +436,12 @@ struct DeviceInfo {
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int max_smem_optin = 0;
-    int fit[2][9][kMaxOutStages + 1] = {};  // [esize==4][in_stages][out_stages], 0 = unknown
+    // [per-warp kernel][esize == 4][in_stages][out_stages]; 0 = not computed
+    int fit[2][2][9][kMaxOutStages + 1] = {};
 };
 
 constexpr int kMaxDevices = 64;
+constexpr int kWarpsPerBlock = 1;  // per-warp pipeline: one warp per block
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
@@ -319,13 +462,14 @@ DeviceInfo &device_info() {
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
             if (e == cudaSuccess)
                 e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
-            // Opt both kernels in to the largest dynamic shared memory once.
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k_tma<uint32_t>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k_tma<uint16_t>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            // Opt the kernels in to the largest dynamic shared memory once.
+            const void *kernels[4] = {reinterpret_cast<const void *>(k_tma<uint32_t>),
+                                      reinterpret_cast<const void *>(k_tma<uint16_t>),
+                                      reinterpret_cast<const void *>(k_tma_warp<uint32_t>),
+                                      reinterpret_cast<const void *>(k_tma_warp<uint16_t>)};
+            for (const void *k : kernels)
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess) {
                 failed.ok = false;
                 failed.err = e;
@@ -339,32 +483,47 @@ DeviceInfo &device_info() {
     return info;
 }
 
+// Dynamic shared memory: 1 KiB of slack to align the buffers to the 128-byte
+// swizzle's 1 KiB pattern, the tile buffers, one 8-byte mbarrier per input slot.
 template <typename T>
-size_t smem_bytes(int in_stages, int out_stages) {
-    // 1 KiB of slack to align the buffers to the 128-byte swizzle's 1 KiB
-    // pattern, then the tiles, then one 8-byte mbarrier per input slot.
+size_t smem_bytes(bool per_warp, int in_stages, int out_stages) {
+    if (per_warp)
+        return 1024 + size_t(kWarpsPerBlock) *
+                          (size_t(in_stages + out_stages) * WarpTile<T>::BYTES + size_t(in_stages) * 8);
     return 1024 + size_t(in_stages + out_stages) * TmaTile<T>::BUF_BYTES + size_t(in_stages) * 8;
 }
 
 template <typename T>
-int resident_ctas(DeviceInfo &dev, int in_stages, int out_stages) {
-    int &slot = dev.fit[sizeof(T) == 4][in_stages][out_stages];
+int resident_ctas(DeviceInfo &dev, bool per_warp, int in_stages, int out_stages) {
+    int &slot = dev.fit[per_warp][sizeof(T) == 4][in_stages][out_stages];
     if (slot == 0) {
         int fit = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &fit, k_tma<T>, kThreads, smem_bytes<T>(in_stages, out_stages)) != cudaSuccess)
-            fit = -1;
-        slot = fit < 1 ? -1 : fit;
+        const size_t smem = smem_bytes<T>(per_warp, in_stages, out_stages);
+        const cudaError_t e =
+            per_warp ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_warp<T>,
+                                                                     32 * kWarpsPerBlock, smem)
+                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma<T>, kThreads, smem);
+        slot = (e != cudaSuccess || fit < 1) ? -1 : fit;
     }
     return slot;
 }
 
-int default_in_stages(size_t esize) { return esize == 4 ? 2 : 2; }
-int default_out_stages(size_t esize) { return esize == 4 ? 2 : 2; }
+// Defaults, the best measured on GB300: per-warp pipeline with 6 box loads
+// in flight and 2 output buffers (fp32, 4 KiB boxes) or 4 loads and 3 output
+// buffers (bf16, 8 KiB boxes); CTA-wide pipeline with 2 + 2.
+int default_in_stages(size_t esize, bool per_warp) {
+    if (per_warp) return esize == 4 ? 6 : 4;
+    return 2;
+}
+int default_out_stages(size_t esize, bool per_warp) {
+    return (per_warp && esize == 2) ? 3 : 2;
+}
 
 template <typename T>
 cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **why) {
-    using L = TmaTile<T>;
+    const bool per_warp = cfg.schedule != 1;
+    const int tile = per_warp ? WarpTile<T>::TILE : TmaTile<T>::TILE;
+    const int boxc = TmaTile<T>::BOXC;  // 128-byte box rows either way
     const int64_t two31 = int64_t(1) << 31, two40 = int64_t(1) << 40;
     if (p.rows >= two31 || p.cols >= two31 || p.batch >= two31) {
         *why = "TMA coordinates are 32-bit: a dimension is 2^31 or more";
@@ -380,16 +539,14 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
         return cudaErrorInvalidValue;
     }
     CUtensorMap tm_in, tm_out;
-    if (!encode_3d(&tm_in, p.in, p.esize, p.cols, p.rows, p.batch, p.ld_in, sin, L::BOXC,
-                   L::TILE) ||
-        !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, L::BOXC,
-                   L::TILE)) {
+    if (!encode_3d(&tm_in, p.in, p.esize, p.cols, p.rows, p.batch, p.ld_in, sin, boxc, tile) ||
+        !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, boxc, tile)) {
         *why = "cuTensorMapEncodeTiled rejected the tensor maps";
         return cudaErrorInvalidValue;
     }
     TmaGeom g{};
-    g.tiles_r = int32_t((p.rows + L::TILE - 1) / L::TILE);
-    g.tiles_c = int32_t((p.cols + L::TILE - 1) / L::TILE);
+    g.tiles_r = int32_t((p.rows + tile - 1) / tile);
+    g.tiles_c = int32_t((p.cols + tile - 1) / tile);
     g.total = p.batch * int64_t(g.tiles_r) * g.tiles_c;
     g.rows = int32_t(p.rows);
     g.cols = int32_t(p.cols);
@@ -400,29 +557,33 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     g.stride_out = sout;
     DeviceInfo &dev = device_info();
     if (!dev.ok) return dev.err;
-    int stages = cfg.stages > 0 ? cfg.stages : default_in_stages(sizeof(T));
-    int out_stages = cfg.out_stages > 0 ? cfg.out_stages : default_out_stages(sizeof(T));
+    const int stages = cfg.stages > 0 ? cfg.stages : default_in_stages(sizeof(T), per_warp);
+    const int out_stages = cfg.out_stages > 0 ? cfg.out_stages : default_out_stages(sizeof(T), per_warp);
     if (stages < 2 || stages > 8 || out_stages < 2 || out_stages > kMaxOutStages) {
         *why = "TMA stage counts out of range";
         return cudaErrorInvalidValue;
     }
     g.in_stages = stages;
     g.out_stages = out_stages;
-    const size_t smem = smem_bytes<T>(stages, out_stages);
+    const size_t smem = smem_bytes<T>(per_warp, stages, out_stages);
     if (smem > size_t(dev.max_smem_optin)) {
         *why = "TMA pipeline does not fit in shared memory; lower the stage count";
         return cudaErrorInvalidValue;
     }
-    const int fit = resident_ctas<T>(dev, stages, out_stages);
+    const int fit = resident_ctas<T>(dev, per_warp, stages, out_stages);
     if (fit < 1) {
         *why = "TMA kernel cannot be resident with this configuration";
         return cudaErrorInvalidValue;
     }
     int per_sm = cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : fit;
     if (per_sm > fit) per_sm = fit;
+    const int64_t units = per_warp ? (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock : g.total;
     int64_t grid = int64_t(dev.sms) * per_sm;
-    if (grid > g.total) grid = g.total;
-    k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
+    if (grid > units) grid = units;
+    if (per_warp)
+        k_tma_warp<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, tm_out, g);
+    else
+        k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
     return cudaGetLastError();
 }
 

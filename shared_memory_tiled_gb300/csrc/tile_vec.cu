@@ -109,7 +109,7 @@ __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int
     return make_uint4(e[0], e[1], e[2], e[3]);
 }
 
-template <typename T, int MR, int MC, bool VEC_IN, bool SHIFT_OUT>
+template <typename T, int MR, int MC, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
 __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
                                                   Geometry g, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
@@ -124,16 +124,15 @@ __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *_
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
 
-    for (int64_t tile = blockIdx.x; tile < g.total; tile += gridDim.x) {
+    // Phase 1a: this thread's chunks of tile `tile`, global -> registers, all
+    // loads issued before any is used.
+    Chunk ld[LOADS];
+    auto load_tile = [&](int64_t tile) {
         int64_t b, tr, tc;
         split_tile(g, tile, diagonal, b, tr, tc);
         const T *src = in + b * g.stride_in;
-        T *dst = out + b * g.stride_out;
         const int64_t r0 = tr * TR, c0 = tc * TC;
         const bool full = (r0 + TR <= g.rows) && (c0 + TC <= g.cols);
-
-        // ---- phase 1: global -> registers -> swizzled shared tile
-        Chunk ld[LOADS];
         const int64_t gc = c0 + lcc * V;
         if (full && VEC_IN) {
 #pragma unroll
@@ -160,13 +159,34 @@ __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *_
                 }
             }
         }
+    };
+
+    // With PREFETCH the grid is persistent and the loads of a block's next
+    // tile are issued as soon as the current tile sits in shared memory, so
+    // they are in flight while the current tile is transposed and stored
+    // ("Shared-memory tiling and bank conflicts", "Protect tile phases": one
+    // stage loads future data while another is consumed).  The registers are
+    // the second buffer; the shared tile is reused once every thread passed
+    // the barrier that ends the previous tile's reads.
+    if (PREFETCH && blockIdx.x < g.total) load_tile(blockIdx.x);
+
+    for (int64_t tile = blockIdx.x; tile < g.total; tile += gridDim.x) {
+        int64_t b, tr, tc;
+        split_tile(g, tile, diagonal, b, tr, tc);
+        T *dst = out + b * g.stride_out;
+        const int64_t r0 = tr * TR, c0 = tc * TC;
+        const bool full = (r0 + TR <= g.rows) && (c0 + TC <= g.cols);
+
+        if (!PREFETCH) load_tile(tile);
         if (tile != blockIdx.x) __syncthreads();  // previous tile fully read
+        // Phase 1b: registers -> swizzled shared tile.
 #pragma unroll
         for (int k = 0; k < LOADS; ++k) {
             const int r = lr + RPP * k;
             smem[r * MC + (lcc ^ ((r / V) & 7))] = ld[k].v;
         }
         __syncthreads();
+        if (PREFETCH && tile + gridDim.x < g.total) load_tile(tile + gridDim.x);
 
         // ---- phase 2: micro-blocks -> registers -> transpose -> global
 #pragma unroll
@@ -228,39 +248,57 @@ __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *_
 
 // Shared memory of one instantiation; above 48 KiB it needs an opt-in, done
 // once per device.
-template <typename T, int MR, int MC, bool VI, bool SO>
+// One instantiation's launch.  Above 48 KiB of shared memory the kernel needs
+// an opt-in, and a persistent grid needs the number of resident blocks per
+// SM: both are found once per device and cached.
+template <typename T, int MR, int MC, bool VI, bool SO, bool PF>
 cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     constexpr size_t smem = size_t(V * MR) * MC * 16;
-    auto kern = k_tile_vec<T, MR, MC, VI, SO>;
-    if (smem > 48 * 1024) {
-        static bool opted[64] = {};
-        static std::mutex mu;
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!opted[dev]) {
-            std::lock_guard<std::mutex> lock(mu);
-            if (!opted[dev]) {
+    auto kern = k_tile_vec<T, MR, MC, VI, SO, PF>;
+    static int resident[64] = {};  // 0 = not set up on that device yet
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!resident[dev]) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!resident[dev]) {
+            if (smem > 48 * 1024) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
                 if (e != cudaSuccess) return e;
-                opted[dev] = true;
             }
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, smem);
+            if (e != cudaSuccess) return e;
+            resident[dev] = n > 0 ? n : 1;
         }
     }
     const Geometry g = make_geometry(p, V * MR, V * MC);
-    kern<<<grid_blocks(g.total), 256, smem, p.stream>>>(static_cast<const T *>(p.in),
-                                                        static_cast<T *>(p.out), g, diagonal);
+    int64_t grid = g.total;
+    if (PF) {
+        const int64_t cap = int64_t(sm_count()) * resident[dev];
+        if (grid > cap) grid = cap;
+    }
+    kern<<<grid_blocks(grid), 256, smem, p.stream>>>(static_cast<const T *>(p.in),
+                                                     static_cast<T *>(p.out), g, diagonal);
     return cudaGetLastError();
 }
 
+template <typename T, int MR, int MC, bool PF>
+cudaError_t launch_align(const Problem &p, bool vec_in, bool vec_out, bool diagonal) {
+    if (vec_in && vec_out) return launch_one<T, MR, MC, true, false, PF>(p, diagonal);
+    if (vec_in) return launch_one<T, MR, MC, true, true, PF>(p, diagonal);
+    if (vec_out) return launch_one<T, MR, MC, false, false, PF>(p, diagonal);
+    return launch_one<T, MR, MC, false, true, PF>(p, diagonal);
+}
+
 template <typename T, int MR, int MC>
-cudaError_t launch_shape(const Problem &p, bool vec_in, bool vec_out, bool diagonal) {
-    if (vec_in && vec_out) return launch_one<T, MR, MC, true, false>(p, diagonal);
-    if (vec_in) return launch_one<T, MR, MC, true, true>(p, diagonal);
-    if (vec_out) return launch_one<T, MR, MC, false, false>(p, diagonal);
-    return launch_one<T, MR, MC, false, true>(p, diagonal);
+cudaError_t launch_shape(const Problem &p, bool vec_in, bool vec_out, bool diagonal,
+                         bool prefetch) {
+    return prefetch ? launch_align<T, MR, MC, true>(p, vec_in, vec_out, diagonal)
+                    : launch_align<T, MR, MC, false>(p, vec_in, vec_out, diagonal);
 }
 
 template <typename T>
@@ -268,14 +306,15 @@ cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecC
                          const char **why) {
     constexpr int V = VecTraits<T>::V;
     const bool diag = cfg.tile_order == 1;
+    const bool pf = cfg.prefetch;
     int mr = cfg.tile_rows ? cfg.tile_rows / V : 16;
     int mc = cfg.tile_cols ? cfg.tile_cols / V : 16;
     if ((cfg.tile_rows % V) || (cfg.tile_cols % V)) mr = mc = 0;
-    if (mr == 16 && mc == 16) return launch_shape<T, 16, 16>(p, vec_in, vec_out, diag);
-    if (mr == 32 && mc == 16) return launch_shape<T, 32, 16>(p, vec_in, vec_out, diag);
-    if (mr == 16 && mc == 32) return launch_shape<T, 16, 32>(p, vec_in, vec_out, diag);
+    if (mr == 16 && mc == 16) return launch_shape<T, 16, 16>(p, vec_in, vec_out, diag, pf);
+    if (mr == 32 && mc == 16) return launch_shape<T, 32, 16>(p, vec_in, vec_out, diag, pf);
+    if (mr == 16 && mc == 32) return launch_shape<T, 16, 32>(p, vec_in, vec_out, diag, pf);
     if constexpr (sizeof(T) == 4) {
-        if (mr == 32 && mc == 32) return launch_shape<T, 32, 32>(p, vec_in, vec_out, diag);
+        if (mr == 32 && mc == 32) return launch_shape<T, 32, 32>(p, vec_in, vec_out, diag, pf);
     }
     *why = sizeof(T) == 4 ? "vector tile shape must be 64 or 128 rows by 64 or 128 columns"
                           : "vector tile shape must be 128x128, 256x128 or 128x256";

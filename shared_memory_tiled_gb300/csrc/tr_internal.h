@@ -24,6 +24,7 @@ struct TmaConfig {
     int stages;        // input pipeline depth, 0 = default
     int tile_order;    // 0 row-major, 1 diagonal
     int out_stages;    // output buffers, 0 = default
+    int schedule;      // 0 default (per-warp), 1 CTA-wide pipeline, 2 per-warp pipelines
 };
 
 // True when the side's base pointer, row pitch and (for batch > 1) plane pitch
@@ -40,6 +41,7 @@ struct VecConfig {
     int tile_order;    // 0 row-major, 1 diagonal
     int tile_rows;     // tile shape in elements, 0 = default
     int tile_cols;
+    bool prefetch;     // persistent blocks that prefetch their next tile
 };
 
 // Launchers: each returns the CUDA error of the launch (cudaSuccess when fine).

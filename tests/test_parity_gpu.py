@@ -54,11 +54,17 @@ def _variants(dtype, aligned):
           dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
           dict(variant=V.TILE_PAD, pad=2), dict(variant=V.TILE_VEC), dict(variant=V.AUTO)]
     vs += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]]
+    vs += [dict(variant=V.TILE_VEC, schedule=2),
+           dict(variant=V.TILE_VEC, schedule=2, tile_rows=VEC_SHAPES[dtype][0][0],
+                tile_cols=VEC_SHAPES[dtype][0][1])]
     if aligned:
         deep = 6 if dtype is U32 else 4   # 8 x 32 KiB bf16 stages would not fit
         vs += [dict(variant=V.TMA), dict(variant=V.TMA, stages=3, out_stages=3),
                dict(variant=V.TMA, stages=2, out_stages=4, ctas_per_sm=1),
-               dict(variant=V.TMA, stages=deep, tile_order=1)]
+               dict(variant=V.TMA, stages=8, tile_order=1),
+               dict(variant=V.TMA, schedule=1), dict(variant=V.TMA, schedule=1, stages=3,
+                                                     out_stages=3),
+               dict(variant=V.TMA, schedule=1, stages=deep, tile_order=1)]
     return vs
 
 
@@ -112,7 +118,8 @@ def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
     for (b, r, c, pi, po, pp) in [(1, 515, 300, 4, 1, 0), (2, 256, 256, 0, 3, 5),
                                   (1, 1025, 263, 9, 0, 0), (3, 130, 129, 7, 2, 1)]:
         x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=r + c)
-        for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC)] + \
+        for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC),
+                   dict(variant=V.TILE_VEC, schedule=2)] + \
                 [dict(variant=V.TILE_VEC, tile_rows=rr, tile_cols=cc) for rr, cc in VEC_SHAPES[dtype]]:
             check(x, prefill, geo, **kw)
 
@@ -127,7 +134,7 @@ def test_unsupported_vector_tile_shape_is_refused():
 def test_tma_stage_count_that_does_not_fit_is_refused():
     x, prefill, geo = case(U16, 1, 128, 128)
     with pytest.raises(B.TransposeError) as e:
-        gpu_out(x, prefill, *geo, variant=V.TMA, stages=8)
+        gpu_out(x, prefill, *geo, variant=V.TMA, schedule=1, stages=8)  # 10 x 32 KiB
     assert e.value.status == B.Status.ERR_UNSUPPORTED
 
 
@@ -184,11 +191,11 @@ def test_workload_full_size(name):
     want = oracle_out(x, prefill, *geo)
     es = w.esize
     aligned = (w.ld_in * es % 16 == 0 and w.ld_out * es % 16 == 0)
-    kws = [dict(variant=V.AUTO), dict(variant=V.TILE_VEC)]
+    kws = [dict(variant=V.AUTO), dict(variant=V.TILE_VEC), dict(variant=V.TILE_VEC, schedule=2)]
     kws += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c)
             for r, c in VEC_SHAPES[U32 if es == 4 else U16]]
     if aligned:
-        kws.append(dict(variant=V.TMA))
+        kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1)]
     if name.startswith("c1"):
         kws += [dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
                 dict(variant=V.TILE_PAD, pad=2), dict(variant=V.NAIVE_ROW),
