@@ -267,7 +267,8 @@ def run_ours(args):
     topts = B.make_options(variant, pad=args.pad, stages=args.stages,
                            ctas_per_sm=args.ctas_per_sm, tile_order=args.tile_order,
                            out_stages=args.out_stages, tile_rows=args.tile_rows,
-                           tile_cols=args.tile_cols, schedule=args.schedule)
+                           tile_cols=args.tile_cols, schedule=args.schedule,
+                           threads=args.threads)
     planned = B.Variant(B.tr_plan_variant(targs, topts))
     lib = B.load()
     ex = lib.tr_transpose_ex
@@ -424,6 +425,7 @@ def main(argv=None):
     ap.add_argument("--out-stages", dest="out_stages", type=int, default=0)
     ap.add_argument("--tile-rows", dest="tile_rows", type=int, default=0)
     ap.add_argument("--tile-cols", dest="tile_cols", type=int, default=0)
+    ap.add_argument("--threads", type=int, default=0, help="vector tile threads per block")
     ap.add_argument("--schedule", type=int, default=0,
                     help="vector tile: 1 = one tile per block, 2 = persistent with prefetch")
     ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)

@@ -60,7 +60,7 @@ class Options(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("tile_order", ctypes.c_int32), ("out_stages", ctypes.c_int32),
                 ("tile_rows", ctypes.c_int32), ("tile_cols", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("schedule", ctypes.c_int32), ("threads", ctypes.c_int32)]
 
 
 class Args(ctypes.Structure):
@@ -150,9 +150,9 @@ def make_args(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, stride_i
 
 
 def make_options(variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0, tile_order=0,
-                 out_stages=0, tile_rows=0, tile_cols=0, schedule=0) -> Options:
+                 out_stages=0, tile_rows=0, tile_cols=0, schedule=0, threads=0) -> Options:
     return Options(int(variant), pad, ctas_per_sm, stages, tile_order, out_stages, tile_rows,
-                   tile_cols, schedule, (ctypes.c_int32 * 1)())
+                   tile_cols, schedule, threads)
 
 
 def tr_transpose_ex(args: Args, opts: Options | None = None) -> int:
@@ -219,7 +219,8 @@ def _geometry(t):
 
 
 def transpose(x, out=None, *, variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0,
-              tile_order=0, out_stages=0, tile_rows=0, tile_cols=0, schedule=0, stream=None):
+              tile_order=0, out_stages=0, tile_rows=0, tile_cols=0, schedule=0, threads=0,
+              stream=None):
     """Transpose the last two dims of a CUDA tensor ``x`` ([R, C] or [B, R, C]).
 
     ``out`` (optional) receives the result and may be a strided view (its row
@@ -244,7 +245,7 @@ def transpose(x, out=None, *, variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages
     args = make_args(x.data_ptr(), out.data_ptr(), dt, b, r, c, ld_in, ld_out, s_in, s_out,
                      stream)
     opts = make_options(variant, pad, ctas_per_sm, stages, tile_order, out_stages, tile_rows,
-                        tile_cols, schedule)
+                        tile_cols, schedule, threads)
     check(tr_transpose_ex(args, opts))
     return out
 

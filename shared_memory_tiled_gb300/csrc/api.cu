@@ -97,8 +97,7 @@ bool options_valid(const tr_options *o) {
     if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
         return false;
     if (o->schedule < 0 || o->schedule > 2) return false;
-    for (int r : o->reserved)
-        if (r != 0) return false;
+    if (o->threads != 0 && o->threads != 128 && o->threads != 256) return false;
     return true;
 }
 
@@ -145,7 +144,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
         case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
         case TR_VARIANT_TILE_VEC: {
             VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
-                          o && o->schedule == 2};
+                          o && o->schedule == 2, o ? o->threads : 0};
             if (cfg.tile_rows == 0 && cfg.tile_cols == 0)
                 auto_vec_shape(p, out16, &cfg.tile_rows, &cfg.tile_cols);
             const char *why = nullptr;
@@ -171,7 +170,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
                 if (auto_mode) {
                     // The planner's first choice could not be encoded (e.g. a
                     // plane pitch the tensor map rejects): take the LSU tile.
-                    VecConfig vc{cfg.tile_order, 0, 0, false};
+                    VecConfig vc{cfg.tile_order, 0, 0, false, 0};
                     auto_vec_shape(p, out16, &vc.tile_rows, &vc.tile_cols);
                     e = launch_tile_vec(p, in16, out16, vc, &why);
                     break;

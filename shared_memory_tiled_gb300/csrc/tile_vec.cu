@@ -3,11 +3,11 @@
 // and a register micro-transpose.
 //
 // A 16-byte chunk holds V = 16 / sizeof(T) elements (4 fp32 or 8 bf16).  The
-// block (256 threads) stages a TR x TC tile, TR = V*MR rows and TC = V*MC
+// block (NT = 128 or 256 threads) stages a TR x TC tile, TR = V*MR rows and TC = V*MC
 // columns: MR x MC micro-blocks of V x V elements, e.g. 64x64 fp32 (16 KiB) or
 // 128x128 bf16 (32 KiB) for MR = MC = 16.
 //
-// Phase 1 (load): thread t takes chunk cc = t % MC of tile rows t / MC + k*256/MC,
+// Phase 1 (load): thread t takes chunk cc = t % MC of tile rows t / MC + k*NT/MC,
 //   with 16-byte global loads (a warp reads whole MC*16-byte row segments), all
 //   of them in flight before the first shared store.
 // Shared layout: chunk cc of tile row r is stored at chunk position
@@ -15,7 +15,7 @@
 //   phases of 8 lanes; it is conflict-free when the 8 lanes hit 8 distinct
 //   positions modulo 8 (each 128 bytes of a row spans all 32 banks once).
 //   Phase-1 stores: 8 lanes = 8 consecutive chunks of one row -> distinct.
-// Phase 2 (transpose): micro-block u = t + 256*j has A = u % MR, C = u / MR and
+// Phase 2 (transpose): micro-block u = t + NT*j has A = u % MR, C = u / MR and
 //   covers tile rows V*A..V*A+V-1 of chunk C.  Its V shared reads (rows V*A+m,
 //   chunk C) land at positions C ^ (A % 8); the 8 lanes of a phase have 8
 //   consecutive A and one C -> distinct.  The register transpose (renaming
@@ -109,15 +109,15 @@ __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int
     return make_uint4(e[0], e[1], e[2], e[3]);
 }
 
-template <typename T, int MR, int MC, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
-__global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
-                                                  Geometry g, bool diagonal) {
+template <typename T, int MR, int MC, int NT, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
+__global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
+                                                 Geometry g, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     constexpr int TR = V * MR, TC = V * MC;  // tile rows / columns in elements
-    constexpr int MB = MR * MC / 256;        // micro-blocks per thread
-    constexpr int RPP = 256 / MC;            // tile rows per load pass
+    constexpr int MB = MR * MC / NT;         // micro-blocks per thread
+    constexpr int RPP = NT / MC;             // tile rows per load pass
     constexpr int LOADS = TR / RPP;          // chunks each thread loads
-    static_assert(MR >= 8 && MR <= 32 && MC >= 8 && 256 % MC == 0 && (MR * MC) % 256 == 0,
+    static_assert(MR >= 8 && MR <= 32 && MC >= 8 && NT % MC == 0 && (MR * MC) % NT == 0,
                   "unsupported tile shape");
     extern __shared__ uint4 smem[];          // TR rows of MC chunks
 
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *_
         // ---- phase 2: micro-blocks -> registers -> transpose -> global
 #pragma unroll
         for (int j = 0; j < MB; ++j) {
-            const int u = t + 256 * j;
+            const int u = t + NT * j;
             const int A = u % MR, C = u / MR;
             Chunk x[V], y[V];
 #pragma unroll
@@ -251,11 +251,11 @@ __global__ void __launch_bounds__(256) k_tile_vec(const T *__restrict__ in, T *_
 // One instantiation's launch.  Above 48 KiB of shared memory the kernel needs
 // an opt-in, and a persistent grid needs the number of resident blocks per
 // SM: both are found once per device and cached.
-template <typename T, int MR, int MC, bool VI, bool SO, bool PF>
+template <typename T, int MR, int MC, int NT, bool VI, bool SO, bool PF>
 cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     constexpr size_t smem = size_t(V * MR) * MC * 16;
-    auto kern = k_tile_vec<T, MR, MC, VI, SO, PF>;
+    auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
     static int resident[64] = {};  // 0 = not set up on that device yet
     static std::mutex mu;
     int dev = 0;
@@ -270,7 +270,7 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
                 if (e != cudaSuccess) return e;
             }
             int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, smem);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, smem);
             if (e != cudaSuccess) return e;
             resident[dev] = n > 0 ? n : 1;
         }
@@ -281,43 +281,58 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
         const int64_t cap = int64_t(sm_count()) * resident[dev];
         if (grid > cap) grid = cap;
     }
-    kern<<<grid_blocks(grid), 256, smem, p.stream>>>(static_cast<const T *>(p.in),
+    kern<<<grid_blocks(grid), NT, smem, p.stream>>>(static_cast<const T *>(p.in),
                                                      static_cast<T *>(p.out), g, diagonal);
     return cudaGetLastError();
 }
 
-template <typename T, int MR, int MC, bool PF>
+template <typename T, int MR, int MC, int NT, bool PF>
 cudaError_t launch_align(const Problem &p, bool vec_in, bool vec_out, bool diagonal) {
-    if (vec_in && vec_out) return launch_one<T, MR, MC, true, false, PF>(p, diagonal);
-    if (vec_in) return launch_one<T, MR, MC, true, true, PF>(p, diagonal);
-    if (vec_out) return launch_one<T, MR, MC, false, false, PF>(p, diagonal);
-    return launch_one<T, MR, MC, false, true, PF>(p, diagonal);
+    if (vec_in && vec_out) return launch_one<T, MR, MC, NT, true, false, PF>(p, diagonal);
+    if (vec_in) return launch_one<T, MR, MC, NT, true, true, PF>(p, diagonal);
+    if (vec_out) return launch_one<T, MR, MC, NT, false, false, PF>(p, diagonal);
+    return launch_one<T, MR, MC, NT, false, true, PF>(p, diagonal);
 }
 
-template <typename T, int MR, int MC>
+template <typename T, int MR, int MC, int NT>
 cudaError_t launch_shape(const Problem &p, bool vec_in, bool vec_out, bool diagonal,
                          bool prefetch) {
-    return prefetch ? launch_align<T, MR, MC, true>(p, vec_in, vec_out, diagonal)
-                    : launch_align<T, MR, MC, false>(p, vec_in, vec_out, diagonal);
+    return prefetch ? launch_align<T, MR, MC, NT, true>(p, vec_in, vec_out, diagonal)
+                    : launch_align<T, MR, MC, NT, false>(p, vec_in, vec_out, diagonal);
 }
 
+// Supported shapes (micro-blocks MR x MC, threads NT).  256 threads for every
+// shape; 128 threads for the smaller tiles, which doubles the loads each
+// thread keeps in flight and lets more blocks share an SM.
 template <typename T>
 cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecConfig &cfg,
                          const char **why) {
     constexpr int V = VecTraits<T>::V;
     const bool diag = cfg.tile_order == 1;
     const bool pf = cfg.prefetch;
+    const int nt = cfg.threads ? cfg.threads : 256;
     int mr = cfg.tile_rows ? cfg.tile_rows / V : 16;
     int mc = cfg.tile_cols ? cfg.tile_cols / V : 16;
     if ((cfg.tile_rows % V) || (cfg.tile_cols % V)) mr = mc = 0;
-    if (mr == 16 && mc == 16) return launch_shape<T, 16, 16>(p, vec_in, vec_out, diag, pf);
-    if (mr == 32 && mc == 16) return launch_shape<T, 32, 16>(p, vec_in, vec_out, diag, pf);
-    if (mr == 16 && mc == 32) return launch_shape<T, 16, 32>(p, vec_in, vec_out, diag, pf);
-    if constexpr (sizeof(T) == 4) {
-        if (mr == 32 && mc == 32) return launch_shape<T, 32, 32>(p, vec_in, vec_out, diag, pf);
+    if (nt == 256) {
+        if (mr == 16 && mc == 16) return launch_shape<T, 16, 16, 256>(p, vec_in, vec_out, diag, pf);
+        if (mr == 32 && mc == 16) return launch_shape<T, 32, 16, 256>(p, vec_in, vec_out, diag, pf);
+        if (mr == 16 && mc == 32) return launch_shape<T, 16, 32, 256>(p, vec_in, vec_out, diag, pf);
+        if constexpr (sizeof(T) == 4) {
+            if (mr == 32 && mc == 32) return launch_shape<T, 32, 32, 256>(p, vec_in, vec_out, diag, pf);
+        }
+    } else if (nt == 128) {
+        if (mr == 16 && mc == 16) return launch_shape<T, 16, 16, 128>(p, vec_in, vec_out, diag, pf);
+        if (mr == 8 && mc == 16) return launch_shape<T, 8, 16, 128>(p, vec_in, vec_out, diag, pf);
+        if constexpr (sizeof(T) == 4) {
+            if (mr == 32 && mc == 16) return launch_shape<T, 32, 16, 128>(p, vec_in, vec_out, diag, pf);
+        }
     }
-    *why = sizeof(T) == 4 ? "vector tile shape must be 64 or 128 rows by 64 or 128 columns"
-                          : "vector tile shape must be 128x128, 256x128 or 128x256";
+    *why = sizeof(T) == 4
+               ? "vector tile: 256 threads take 64x64, 128x64, 64x128 or 128x128 fp32 tiles; "
+                 "128 threads take 64x64, 32x64 or 128x64"
+               : "vector tile: 256 threads take 128x128, 256x128 or 128x256 bf16 tiles; "
+                 "128 threads take 128x128 or 64x128";
     return cudaErrorInvalidValue;
 }
 

@@ -133,8 +133,7 @@ def test_planner(lib):
 def test_ex_rejects_bad_options_and_reserved_fields(lib):
     a = B.make_args(FAKE_IN, FAKE_OUT, B.DType.F32, 1, 4, 4, 4, 4)
     assert B.tr_transpose_ex(a, B.make_options(variant=42)) == B.Status.ERR_UNSUPPORTED
-    o = B.make_options()
-    o.reserved[0] = 3
+    o = B.make_options(threads=64)
     assert B.tr_transpose_ex(a, o) == B.Status.ERR_UNSUPPORTED
     a.reserved = 1
     assert B.tr_transpose_ex(a, None) == B.Status.ERR_UNSUPPORTED

@@ -47,6 +47,7 @@ SHAPES = [(1, 1), (1, 300), (300, 1), (64, 64), (128, 128), (200, 333), (257, 12
 
 
 VEC_SHAPES = {U32: [(128, 64), (64, 128), (128, 128)], U16: [(256, 128), (128, 256)]}
+VEC_128 = {U32: [(64, 64), (32, 64), (128, 64)], U16: [(128, 128), (64, 128)]}
 
 
 def _variants(dtype, aligned):
@@ -54,6 +55,7 @@ def _variants(dtype, aligned):
           dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
           dict(variant=V.TILE_PAD, pad=2), dict(variant=V.TILE_VEC), dict(variant=V.AUTO)]
     vs += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]]
+    vs += [dict(variant=V.TILE_VEC, threads=128, tile_rows=r, tile_cols=c) for r, c in VEC_128[dtype]]
     vs += [dict(variant=V.TILE_VEC, schedule=2),
            dict(variant=V.TILE_VEC, schedule=2, tile_rows=VEC_SHAPES[dtype][0][0],
                 tile_cols=VEC_SHAPES[dtype][0][1])]
@@ -120,6 +122,8 @@ def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
         x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=r + c)
         for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC),
                    dict(variant=V.TILE_VEC, schedule=2)] + \
+                [dict(variant=V.TILE_VEC, threads=128, tile_rows=rr, tile_cols=cc)
+                 for rr, cc in VEC_128[dtype]] + \
                 [dict(variant=V.TILE_VEC, tile_rows=rr, tile_cols=cc) for rr, cc in VEC_SHAPES[dtype]]:
             check(x, prefill, geo, **kw)
 
@@ -194,6 +198,8 @@ def test_workload_full_size(name):
     kws = [dict(variant=V.AUTO), dict(variant=V.TILE_VEC), dict(variant=V.TILE_VEC, schedule=2)]
     kws += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c)
             for r, c in VEC_SHAPES[U32 if es == 4 else U16]]
+    kws += [dict(variant=V.TILE_VEC, threads=128, tile_rows=r, tile_cols=c)
+            for r, c in VEC_128[U32 if es == 4 else U16]]
     if aligned:
         kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1)]
     if name.startswith("c1"):
