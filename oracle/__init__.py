@@ -64,6 +64,10 @@ def _load():
                 fn.restype = None
             lib.oracle_copy_bytes.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64]
             lib.oracle_copy_bytes.restype = None
+            for name in ("oracle_transpose_inplace_u32", "oracle_transpose_inplace_u16"):
+                fn = getattr(lib, name)
+                fn.argtypes = [ctypes.c_void_p, _I64, _I64, _I64, _I64]
+                fn.restype = None
             _lib = lib
     return _lib
 
@@ -115,3 +119,21 @@ def copy_bytes(x: np.ndarray, out: np.ndarray) -> np.ndarray:
         raise ValueError("size mismatch")
     _load().oracle_copy_bytes(x.ctypes.data, out.ctypes.data, x.nbytes)
     return out
+
+
+def transpose_inplace(data: np.ndarray, *, batch: int = 1, n: int, ld: int | None = None,
+                      stride: int | None = None) -> np.ndarray:
+    """Transpose each n x n plane of ``data`` in place (element (i, j) swaps with
+    (j, i)); padding between ``n`` and ``ld`` and between planes is untouched."""
+    ld = n if ld is None else ld
+    stride = n * ld if stride is None else stride
+    if data.dtype not in (np.uint32, np.uint16) or data.ndim != 1 or not data.flags.c_contiguous:
+        raise TypeError("oracle works on flat uint32 or uint16 bit patterns")
+    if min(batch, n) < 0 or ld < n or (batch > 1 and stride < (n - 1) * ld + n):
+        raise ValueError("bad sizes")
+    if data.size < _extent(batch, n, n, ld, stride):
+        raise ValueError("buffer smaller than its logical extent")
+    lib = _load()
+    name = "oracle_transpose_inplace_" + ("u32" if data.dtype == np.uint32 else "u16")
+    getattr(lib, name)(data.ctypes.data, batch, n, ld, stride)
+    return data

@@ -98,3 +98,36 @@ void oracle_copy_bytes(const uint8_t *in, uint8_t *out, int64_t bytes)
     for (int64_t k = 0; k < bytes; ++k)
         out[k] = in[k];
 }
+
+/* ---- in-place transpose of square planes -------------------------------
+ * The same result written over the input: plane b of an n x n matrix with
+ * row pitch ld becomes its transpose, element (i, j) exchanging places with
+ * element (j, i) for every i < j; diagonal and padding elements stay put.   */
+
+void oracle_transpose_inplace_u32(uint32_t *data, int64_t batch, int64_t n, int64_t ld,
+                                  int64_t stride)
+{
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t i = 0; i < n; ++i)
+            for (int64_t j = i + 1; j < n; ++j) {
+                uint32_t *p = data + b * stride + i * ld + j;
+                uint32_t *q = data + b * stride + j * ld + i;
+                uint32_t tmp = *p;
+                *p = *q;
+                *q = tmp;
+            }
+}
+
+void oracle_transpose_inplace_u16(uint16_t *data, int64_t batch, int64_t n, int64_t ld,
+                                  int64_t stride)
+{
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t i = 0; i < n; ++i)
+            for (int64_t j = i + 1; j < n; ++j) {
+                uint16_t *p = data + b * stride + i * ld + j;
+                uint16_t *q = data + b * stride + j * ld + i;
+                uint16_t tmp = *p;
+                *p = *q;
+                *q = tmp;
+            }
+}

@@ -41,3 +41,7 @@ def fixture_arrays(path, dtype, pad_in, pad_out):
 
 def transpose_fixtures():
     return sorted(glob.glob(os.path.join(GOLDEN_DIR, "transpose_*.txt")))
+
+
+def inplace_fixtures():
+    return sorted(glob.glob(os.path.join(GOLDEN_DIR, "inplace_*.txt")))

@@ -135,3 +135,50 @@ def test_oracle_rejects_bad_sizes():
         oracle.transpose(x, np.zeros(10, dtype=np.uint32), rows=3, cols=4)
     with pytest.raises(TypeError):
         oracle.transpose(x.view(np.float32), np.zeros(10, np.float32), rows=2, cols=5)
+
+
+# --- in-place transpose ----------------------------------------------------------------
+
+import golden_io  # noqa: E402
+
+
+def test_inplace_golden():
+    for path in golden_io.inplace_fixtures():
+        for dt in (np.uint32, np.uint16):
+            p, x, want = golden_io.fixture_arrays(path, dt, pins.PAD_IN[dt], pins.PAD_IN[dt])
+            oracle.transpose_inplace(x, batch=p["batch"], n=p["rows"], ld=p["ld_in"],
+                                     stride=p["stride_in"])
+            assert np.array_equal(x, want), path
+
+
+@pytest.mark.parametrize("dt", [np.uint32, np.uint16])
+def test_inplace_matches_out_of_place_and_is_an_involution(dt):
+    rng = np.random.default_rng(1)
+    for batch, n, pad, ppad in [(1, 1, 0, 0), (1, 7, 0, 0), (2, 33, 3, 5), (3, 64, 0, 0),
+                                (1, 130, 6, 0), (2, 257, 1, 3)]:
+        ld, stride = n + pad, n * (n + pad) + ppad
+        size = (batch - 1) * stride + (n - 1) * ld + n if n else 0
+        x = rng.integers(0, np.iinfo(dt).max, size, dtype=dt, endpoint=True)
+        want = x.copy()
+        oracle.transpose(x, want, batch=batch, rows=n, cols=n, ld_in=ld, ld_out=ld,
+                         stride_in=stride, stride_out=stride)
+        got = x.copy()
+        oracle.transpose_inplace(got, batch=batch, n=n, ld=ld, stride=stride)
+        assert np.array_equal(got, want)
+        oracle.transpose_inplace(got, batch=batch, n=n, ld=ld, stride=stride)
+        assert np.array_equal(got, x)
+
+
+def test_inplace_brute_force_tiny():
+    for n in range(0, 7):
+        for pad in (0, 2):
+            ld = n + pad
+            size = max(0, (n - 1) * ld + n)
+            x = np.arange(size, dtype=np.uint32)
+            got = x.copy()
+            oracle.transpose_inplace(got, n=n, ld=ld)
+            want = x.copy()
+            for i in range(n):
+                for j in range(n):
+                    want[j * ld + i] = x[i * ld + j]
+            assert np.array_equal(got, want)
