@@ -153,6 +153,22 @@ tr_status tr_transpose_batched_bf16(const void *in, void *out, int64_t batch, in
  * arguments (e.g. TMA with a pitch that is not a multiple of 16 bytes). */
 tr_status tr_transpose_ex(const tr_args *args, const tr_options *opts);
 
+/* In-place transpose of `batch` square n x n planes of fp32 bit patterns:
+ * element (i, j) of plane b (at data + b*stride + i*ld + j) exchanges places
+ * with element (j, i); the diagonal and all pitch padding stay as they were.
+ * Requires ld >= n and, for batch > 1, stride >= (n-1)*ld + n (stride is
+ * ignored when batch == 1).  Each pair of mirror tiles is read completely
+ * before either is written, so the call is safe on one buffer; the planes
+ * of one call must not overlap each other.  Same errors as above (no
+ * TR_ERR_OVERLAP: aliasing is the point).  Not part of the pages' kernels:
+ * it is the square special case in which the output buffer is the input. */
+tr_status tr_transpose_inplace_f32(float *data, int64_t batch, int64_t n, int64_t ld,
+                                   int64_t stride, tr_stream_t stream);
+
+/* In-place transpose of square planes of bf16 bit patterns; as above. */
+tr_status tr_transpose_inplace_bf16(void *data, int64_t batch, int64_t n, int64_t ld,
+                                    int64_t stride, tr_stream_t stream);
+
 /* Device-to-device copy of `bytes` bytes, the bandwidth ceiling the transpose
  * is compared against ("Shared memory and the bank conflict", section "What to
  * record": the transpose timings sit next to a copy of the same bytes).

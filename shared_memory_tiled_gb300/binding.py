@@ -87,6 +87,8 @@ SIGNATURES = {
     "tr_transpose_batched_bf16": ([VP, VP, I64, I64, I64, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_transpose_ex": ([ctypes.POINTER(Args), ctypes.POINTER(Options)], ctypes.c_int),
     "tr_copy": ([VP, VP, ctypes.c_size_t, VP], ctypes.c_int),
+    "tr_transpose_inplace_f32": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
+    "tr_transpose_inplace_bf16": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_plan_variant": ([ctypes.POINTER(Args), ctypes.POINTER(Options)], ctypes.c_int32),
     "tr_device_status": ([], ctypes.c_int),
     "tr_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -157,6 +159,14 @@ def make_options(variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages=0, tile_orde
 
 def tr_transpose_ex(args: Args, opts: Options | None = None) -> int:
     return _call("tr_transpose_ex", ctypes.byref(args), ctypes.byref(opts) if opts else None)
+
+
+def tr_transpose_inplace_f32(ptr, batch, n, ld, stride, stream=0) -> int:
+    return _call("tr_transpose_inplace_f32", ptr, batch, n, ld, stride, stream)
+
+
+def tr_transpose_inplace_bf16(ptr, batch, n, ld, stride, stream=0) -> int:
+    return _call("tr_transpose_inplace_bf16", ptr, batch, n, ld, stride, stream)
 
 
 def tr_copy(in_ptr, out_ptr, nbytes, stream=0) -> int:
@@ -262,3 +272,19 @@ def copy(src, dst, stream=None):
         stream = torch.cuda.current_stream(src.device).cuda_stream
     check(tr_copy(src.data_ptr(), dst.data_ptr(), n, stream))
     return dst
+
+
+def transpose_(x, stream=None):
+    """Transpose the last two (equal) dims of a CUDA tensor in place."""
+    import torch
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor: the library has no CPU path")
+    dt = _dtype_of(x)
+    b, r, c, ld, s = _geometry(x)
+    if r != c:
+        raise ValueError("in-place transpose needs square planes")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    f = tr_transpose_inplace_f32 if dt == DType.F32 else tr_transpose_inplace_bf16
+    check(f(x.data_ptr(), b, r, ld, s, stream))
+    return x

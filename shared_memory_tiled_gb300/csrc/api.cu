@@ -207,6 +207,28 @@ tr_args make_args(const void *in, void *out, tr_dtype dt, int64_t batch, int64_t
     return a;
 }
 
+tr_status run_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
+                      int64_t stride, tr_stream_t stream) {
+    if (batch < 0 || n < 0) return TR_ERR_BAD_DIM;
+    if (batch == 0 || n == 0) return TR_OK;
+    if (!data) return TR_ERR_NULL;
+    if (ld < n) return TR_ERR_BAD_LD;
+    int64_t plane, ext, bytes;
+    if (!mul_add(n - 1, ld, n, &plane)) return TR_ERR_BAD_DIM;
+    if (batch > 1 && stride < plane) return TR_ERR_BAD_LD;
+    if (!side_extent(batch, n, n, ld, stride, &ext) || !mul_add(ext, esize, 0, &bytes))
+        return TR_ERR_BAD_DIM;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(data);
+    if (d0 + uintptr_t(bytes) < d0) return TR_ERR_BAD_DIM;
+    const cudaError_t e = launch_inplace(data, esize, batch, n, ld, batch > 1 ? stride : n * ld,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_error("in-place transpose launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
 }  // namespace
 
 int sm_count() {
@@ -257,6 +279,16 @@ tr_status tr_transpose_batched_bf16(const void *in, void *out, int64_t batch, in
 
 tr_status tr_transpose_ex(const tr_args *args, const tr_options *opts) {
     return tr::run(args, opts);
+}
+
+tr_status tr_transpose_inplace_f32(float *data, int64_t batch, int64_t n, int64_t ld,
+                                   int64_t stride, tr_stream_t stream) {
+    return tr::run_inplace(data, 4, batch, n, ld, stride, stream);
+}
+
+tr_status tr_transpose_inplace_bf16(void *data, int64_t batch, int64_t n, int64_t ld,
+                                    int64_t stride, tr_stream_t stream) {
+    return tr::run_inplace(data, 2, batch, n, ld, stride, stream);
 }
 
 tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream) {

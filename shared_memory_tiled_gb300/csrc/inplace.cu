@@ -1,0 +1,161 @@
+// In-place transpose of square planes: data[b][j][i] <- data[b][i][j].
+//
+// The out-of-place kernels read one tile and write its transpose elsewhere.
+// In place, the transpose of tile (ti, tj) lands where tile (tj, ti) lives, so
+// one block owns each unordered pair of tiles: it reads BOTH tiles into
+// registers, stages them in two swizzled shared tiles, and only after the
+// barrier writes each one's transpose over the other ("Shared memory and the
+// bank conflict", "The barrier": nothing may be written before every thread's
+// reads are in).  A diagonal tile is its own partner.  No other block reads or
+// writes either tile, so blocks never race.
+//
+// Layout and lane mapping are those of the vectorised swizzled tile (tile_vec.cu):
+// a 16V x 16V tile (64x64 fp32, 128x128 bf16), chunk cc of tile row r stored at
+// chunk position cc ^ ((r / V) % 8), 256 threads, 16-byte loads and stores and a
+// register micro-transpose; VEC = false moves single elements (any alignment).
+//
+// Blocks walk a batch * T * T grid of tile coordinates (T tiles per side) and
+// skip the lower triangle, so each pair is taken exactly once.
+#include "tile_geom.cuh"
+#include "tr_internal.h"
+#include "vec_common.cuh"
+
+#include <mutex>
+
+namespace tr {
+namespace {
+
+struct InplaceGeom {
+    int64_t batch, n, ld, stride;
+    int64_t tiles;  // tiles per side
+    int64_t total;  // batch * tiles * tiles
+};
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGeom g) {
+    constexpr int V = VecTraits<T>::V;
+    constexpr int TILE = 16 * V;
+    constexpr int LOADS = V;        // 16 tile rows per load pass, TILE rows
+    extern __shared__ uint4 smem[]; // two tiles of TILE rows x 16 chunks
+    uint4 *tile0 = smem, *tile1 = smem + TILE * 16;
+
+    const int t = threadIdx.x;
+    const int lcc = t & 15, lr = t >> 4;  // phase 1: chunk and first row
+    const int A = t & 15, C = t >> 4;     // phase 2: micro-block
+
+    bool first = true;
+    for (int64_t w = blockIdx.x; w < g.total; w += gridDim.x) {
+        const int64_t per_plane = g.tiles * g.tiles;
+        const int64_t b = w / per_plane;
+        const int64_t rem = w - b * per_plane;
+        const int64_t ti = rem / g.tiles, tj = rem - ti * g.tiles;
+        if (ti > tj) continue;  // the pair is handled at (tj, ti)
+        T *plane = data + b * g.stride;
+        const bool diag = ti == tj;
+        const int64_t r0 = ti * TILE, c0 = tj * TILE;  // tile (ti, tj); partner at (c0, r0)
+        const bool full = r0 + TILE <= g.n && c0 + TILE <= g.n;
+
+        // Phase 1: both tiles, global -> registers.
+        Chunk x0[LOADS], x1[LOADS];
+        auto load = [&](int64_t rr0, int64_t cc0, Chunk (&ld)[LOADS]) {
+            const int64_t gc = cc0 + lcc * V;
+#pragma unroll
+            for (int k = 0; k < LOADS; ++k) {
+                const int64_t gr = rr0 + lr + 16 * k;
+                if (VEC && (full || (gr < g.n && gc + V <= g.n))) {
+                    ld[k].v = *reinterpret_cast<const uint4 *>(plane + gr * g.ld + gc);
+                } else {
+                    T e[V];
+#pragma unroll
+                    for (int q = 0; q < V; ++q)
+                        e[q] = (gr < g.n && gc + q < g.n) ? plane[gr * g.ld + gc + q] : T(0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (sizeof(T) == 4)
+                            ld[k].w[q] = uint32_t(e[q]);
+                        else
+                            ld[k].w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                    }
+                }
+            }
+        };
+        load(r0, c0, x0);
+        if (!diag) load(c0, r0, x1);
+        if (!first) __syncthreads();  // previous pair fully read from shared memory
+        first = false;
+#pragma unroll
+        for (int k = 0; k < LOADS; ++k) {
+            const int r = lr + 16 * k;
+            tile0[r * 16 + (lcc ^ ((r / V) & 7))] = x0[k].v;
+            if (!diag) tile1[r * 16 + (lcc ^ ((r / V) & 7))] = x1[k].v;
+        }
+        __syncthreads();  // every read of both tiles is in before any write
+
+        // Phase 2: tile0 (at r0, c0) goes to (c0, r0); tile1 (at c0, r0) to (r0, c0).
+        auto store = [&](const uint4 *tile, int64_t dr0, int64_t dc0) {
+            Chunk xv[V], yv[V];
+#pragma unroll
+            for (int m = 0; m < V; ++m) xv[m].v = tile[(V * A + m) * 16 + (C ^ (A & 7))];
+            micro_transpose(xv, yv);
+            const int64_t oc = dc0 + V * A;
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                const int64_t orow = dr0 + V * C + m;
+                if (!full && orow >= g.n) break;
+                T *row = plane + orow * g.ld;
+                if (VEC && (full || oc + V <= g.n)) {
+                    *reinterpret_cast<uint4 *>(row + oc) = yv[m].v;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < V; ++q)
+                        if (oc + q < g.n) row[oc + q] = elem<T>(yv[m], q);
+                }
+            }
+        };
+        store(tile0, c0, r0);
+        if (!diag) store(tile1, r0, c0);
+    }
+}
+
+template <typename T, bool VEC>
+cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
+    constexpr int V = VecTraits<T>::V;
+    constexpr size_t smem = 2 * size_t(16 * V) * 16 * 16;
+    auto kern = k_inplace<T, VEC>;
+    if (smem > 48 * 1024) {
+        static bool opted[64] = {};
+        static std::mutex mu;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!opted[dev]) {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!opted[dev]) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                if (e != cudaSuccess) return e;
+                opted[dev] = true;
+            }
+        }
+    }
+    kern<<<grid_blocks(g.total), 256, smem, stream>>>(data, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
+                           int64_t stride, cudaStream_t stream) {
+    const int V = 16 / esize;
+    InplaceGeom g{batch, n, ld, stride, 0, 0};
+    g.tiles = (n + 16 * V - 1) / (16 * V);
+    g.total = batch * g.tiles * g.tiles;
+    const bool vec = side_aligned16(data, ld, stride, batch, esize);
+    if (esize == 4)
+        return vec ? launch_typed<uint32_t, true>(static_cast<uint32_t *>(data), g, stream)
+                   : launch_typed<uint32_t, false>(static_cast<uint32_t *>(data), g, stream);
+    return vec ? launch_typed<uint16_t, true>(static_cast<uint16_t *>(data), g, stream)
+               : launch_typed<uint16_t, false>(static_cast<uint16_t *>(data), g, stream);
+}
+
+}  // namespace tr

@@ -146,3 +146,15 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     with pytest.raises(B.LibraryMissing):
         B.load(str(tmp_path / "nope.so"))
     monkeypatch.setattr(B, "_lib", None)
+
+
+@pytest.mark.parametrize("fn", ["tr_transpose_inplace_f32", "tr_transpose_inplace_bf16"])
+def test_inplace_argument_errors(lib, fn):
+    f = getattr(B, fn)
+    assert f(FAKE_IN, -1, 4, 4, 16) == B.Status.ERR_BAD_DIM
+    assert f(FAKE_IN, 1, -4, 4, 16) == B.Status.ERR_BAD_DIM
+    assert f(0, 1, 4, 4, 16) == B.Status.ERR_NULL
+    assert f(FAKE_IN, 1, 5, 4, 16) == B.Status.ERR_BAD_LD
+    assert f(FAKE_IN, 2, 4, 4, 15) == B.Status.ERR_BAD_LD
+    assert f(FAKE_IN, 1, 1 << 40, 1 << 40, 0) == B.Status.ERR_BAD_DIM
+    assert f(0, 0, 4, 4, 16) == B.Status.OK and f(0, 3, 0, 0, 0) == B.Status.OK
