@@ -64,6 +64,9 @@ def _load():
                 fn.restype = None
             lib.oracle_copy_bytes.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64]
             lib.oracle_copy_bytes.restype = None
+            lib.oracle_operand_tiles_u32.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64, _I64,
+                                                     _I64, _I64, _I64]
+            lib.oracle_operand_tiles_u32.restype = None
             for name in ("oracle_transpose_inplace_u32", "oracle_transpose_inplace_u16"):
                 fn = getattr(lib, name)
                 fn.argtypes = [ctypes.c_void_p, _I64, _I64, _I64, _I64]
@@ -137,3 +140,18 @@ def transpose_inplace(data: np.ndarray, *, batch: int = 1, n: int, ld: int | Non
     name = "oracle_transpose_inplace_" + ("u32" if data.dtype == np.uint32 else "u16")
     getattr(lib, name)(data.ctypes.data, batch, n, ld, stride)
     return data
+
+
+def operand_tiles(a: np.ndarray, out: np.ndarray, *, m: int, k: int, lda: int, bm: int,
+                  bk: int) -> np.ndarray:
+    """Blocked transposed operand tiles of a row-major M x K matrix (fp32 bits):
+    tile (mt, kt) of ``out`` holds As[k][m] = A[mt*bm + m][kt*bk + k], unpadded,
+    tiles in (mt, kt) row-major order.  M and K must be multiples of bm, bk."""
+    if a.dtype != np.uint32 or out.dtype != np.uint32:
+        raise TypeError("operand tiles are fp32 bit patterns (uint32)")
+    if m % bm or k % bk or lda < k or min(m, k, bm, bk) <= 0:
+        raise ValueError("bad sizes")
+    if a.size < (m - 1) * lda + k or out.size < m * k:
+        raise ValueError("buffer smaller than its extent")
+    _load().oracle_operand_tiles_u32(a.ctypes.data, out.ctypes.data, m, k, lda, bm, bk)
+    return out

@@ -131,3 +131,26 @@ void oracle_transpose_inplace_u16(uint16_t *data, int64_t batch, int64_t n, int6
                 *q = tmp;
             }
 }
+
+/* ---- transposed operand tiles ------------------------------------------
+ * "Padded Shared Memory: Eliminating Bank Conflicts", sections "How Shared
+ * Memory Is Addressed" and "The Fix Is One Constant": the SGEMM kernel loads
+ * a BM x BK tile of A (rows m, columns k of a row-major M x K matrix with row
+ * pitch lda) and stores it transposed in shared memory, As[k][m] = A[m][k]
+ * (the padding of the As row pitch changes only where the words sit, never
+ * their values).  The stage on its own writes every tile's As, unpadded, to
+ * a blocked output: tile (mt, kt) at ((mt * K/BK) + kt) * BK*BM, element
+ * (k, m) at k*BM + m.  M and K are multiples of BM and BK.                 */
+
+void oracle_operand_tiles_u32(const uint32_t *a, uint32_t *out, int64_t m_rows, int64_t k_cols,
+                              int64_t lda, int64_t bm, int64_t bk)
+{
+    const int64_t tiles_k = k_cols / bk;
+    for (int64_t mt = 0; mt < m_rows / bm; ++mt)
+        for (int64_t kt = 0; kt < tiles_k; ++kt) {
+            uint32_t *as = out + (mt * tiles_k + kt) * bk * bm;
+            for (int64_t k = 0; k < bk; ++k)
+                for (int64_t m = 0; m < bm; ++m)
+                    as[k * bm + m] = a[(mt * bm + m) * lda + kt * bk + k];
+        }
+}

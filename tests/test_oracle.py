@@ -182,3 +182,33 @@ def test_inplace_brute_force_tiny():
                 for j in range(n):
                     want[j * ld + i] = x[i * ld + j]
             assert np.array_equal(got, want)
+
+
+# --- transposed operand tiles ("Padded Shared Memory", the As store) ---------------------
+
+@pytest.mark.parametrize("bm,bk", [(128, 16), (128, 8), (64, 32), (2, 4)])
+def test_operand_tiles_match_numpy_blocked_transpose(bm, bk):
+    m, k, lda = 2 * bm, 3 * bk, 3 * bk + 5
+    rng = np.random.default_rng(bm + bk)
+    a = rng.integers(0, 1 << 32, (m - 1) * lda + k, dtype=np.uint64).astype(np.uint32)
+    out = np.zeros(m * k, dtype=np.uint32)
+    oracle.operand_tiles(a, out, m=m, k=k, lda=lda, bm=bm, bk=bk)
+    dense = np.lib.stride_tricks.as_strided(a, shape=(m, k), strides=(lda * 4, 4))
+    want = dense.reshape(m // bm, bm, k // bk, bk).transpose(0, 2, 3, 1)  # [mt][kt][k][m]
+    assert np.array_equal(out.reshape(m // bm, k // bk, bk, bm), want)
+
+
+def test_operand_tiles_index_closed_form_and_hand_example():
+    # A is 2x4 (lda 4) holding its own linear index; BM = 2, BK = 2 gives two
+    # tiles, each the transpose of a 2x2 block: [[0,4],[1,5]] and [[2,6],[3,7]].
+    a = np.arange(8, dtype=np.uint32)
+    out = np.zeros(8, dtype=np.uint32)
+    oracle.operand_tiles(a, out, m=2, k=4, lda=4, bm=2, bk=2)
+    assert out.tolist() == [0, 4, 1, 5, 2, 6, 3, 7]
+    m, k, bm, bk = 8, 12, 4, 3
+    a = np.arange(m * k, dtype=np.uint32)
+    out = np.zeros(m * k, dtype=np.uint32)
+    oracle.operand_tiles(a, out, m=m, k=k, lda=k, bm=bm, bk=bk)
+    mt, kt, kk, mm = np.indices((m // bm, k // bk, bk, bm))
+    assert np.array_equal(out.reshape(m // bm, k // bk, bk, bm),
+                          ((mt * bm + mm) * k + kt * bk + kk).astype(np.uint32))
