@@ -56,11 +56,12 @@ def read_peaks():
 # Source files each kernel is built from (the hash of these decides whether a
 # recorded ncu traffic figure still describes the kernel that runs).
 KERNEL_SOURCES = {
-    "k_tile_vec": ["tile_vec.cu", "tile_geom.cuh", "tr_internal.h"],
+    "k_tile_vec": ["tile_vec.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h"],
     "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
     "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_copy_aligned": ["copy.cu", "tr_internal.h"],
+    "k_inplace": ["inplace.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h"],
 }
 
 
@@ -274,9 +275,13 @@ def run_ours(args):
     ex = lib.tr_transpose_ex
     import ctypes
     pa, po = ctypes.byref(targs), ctypes.byref(topts)
+    inplace = args.op == "inplace"
+    if inplace and (w.rows != w.cols or w.batch != 1):
+        raise SystemExit("bench: the in-place transpose needs a square single-plane workload")
+    ipf = lib.tr_transpose_inplace_f32 if w.esize == 4 else lib.tr_transpose_inplace_bf16
 
     def step():
-        st = ex(pa, po)
+        st = ipf(d_in.data_ptr(), 1, w.rows, w.ld_in, w.sin, sptr) if inplace else ex(pa, po)
         if st:
             B.check(st)
 
@@ -333,14 +338,21 @@ def run_ours(args):
     kernel_gbs = w.algorithmic_bytes / (statistics.fmean(per_ms) / 1e3) / 1e9
 
     # ---- parity guard on the timed output: sampled positions vs the definition
-    got = d_out.cpu().numpy().view(x_host.dtype)
     rng = np.random.default_rng(123)
     n = 4096
     bb = rng.integers(0, w.batch, n)
     ii = rng.integers(0, w.rows, n)
     jj = rng.integers(0, w.cols, n)
     src = x_host[bb * w.sin + ii * w.ld_in + jj]
-    dst = got[bb * w.sout + jj * w.ld_out + ii]
+    if inplace:
+        # every step transposes the buffer in place: an even number of steps
+        # (warm-up, timed and clock-window runs together) restores the input
+        got = d_in.cpu().numpy().view(x_host.dtype)
+        total_runs = args.warmup + args.steps + (reps if extra_window else 0)
+        dst = got[ii * w.ld_in + jj] if total_runs % 2 == 0 else got[jj * w.ld_in + ii]
+    else:
+        got = d_out.cpu().numpy().view(x_host.dtype)
+        dst = got[bb * w.sout + jj * w.ld_out + ii]
     if not np.array_equal(src, dst):
         raise SystemExit("bench: the timed output differs from the input at sampled positions")
 
@@ -358,15 +370,26 @@ def run_ours(args):
         step()
         pin_out.copy_(d_out, non_blocking=True)
 
-    e_total, _ = timed(e2e_step, k_e2e, 2)
+    def e2e_inplace_step():
+        d_in.copy_(pin_in, non_blocking=True)
+        step()
+        pin_out.copy_(d_in, non_blocking=True)
+
+    e_total, _ = timed(e2e_inplace_step if inplace else e2e_step, k_e2e, 2)
     e_total = max_over_ranks(e_total, world)
     e2e_gbs = w.algorithmic_bytes * k_e2e * world / (e_total / 1e3) / 1e9
-    if not np.array_equal(pin_out.numpy().view(x_host.dtype)[:64], got[:64]):
-        raise SystemExit("bench: end-to-end output differs from the device-timed output")
+    # every end-to-end step uploads the input and transposes it once
+    e2e_got = pin_out.numpy().view(x_host.dtype)
+    e2e_dst = (e2e_got[jj * w.ld_in + ii] if inplace
+               else e2e_got[bb * w.sout + jj * w.ld_out + ii])
+    if not np.array_equal(e2e_dst, src):
+        raise SystemExit("bench: end-to-end output differs from the transposed input")
 
     peak, peak_kind = read_peaks()
     kname = {B.Variant.TMA: "k_tma", B.Variant.TILE_VEC: "k_tile_vec",
              B.Variant.TILE_PAD: "k_tile_pad"}.get(planned, str(planned.name).lower())
+    if inplace:
+        kname = "k_inplace"
     traffic, traffic_note = recorded_traffic(kname, w.name)
 
     line = {
@@ -374,8 +397,10 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u32" if w.esize == 4 else "u16", "data": "synthetic",
-        "config": {"workload": w.name, "description": W.DESCRIPTION[w.name],
-                   "bytes_per_step": w.algorithmic_bytes, "variant": planned.name,
+        "config": {"workload": w.name + ("_inplace" if inplace else ""),
+                   "description": W.DESCRIPTION[w.name] + (", transposed in place" if inplace else ""),
+                   "bytes_per_step": w.algorithmic_bytes,
+                   "variant": "INPLACE" if inplace else planned.name,
                    "l2": "no flush: input and output each larger than the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_measured": round(100 * gbs / world / peak, 2),
@@ -416,6 +441,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(W.WORKLOADS), default="c2")
+    ap.add_argument("--op", choices=["transpose", "inplace"], default="transpose",
+                    help="out-of-place transpose (default) or in-place square transpose")
     ap.add_argument("--variant", default="auto",
                     choices=["auto", "naive_row", "naive_col", "tile_pad", "tile_vec", "tma"])
     ap.add_argument("--pad", type=int, default=1)

@@ -175,6 +175,36 @@ tr_status tr_transpose_inplace_bf16(void *data, int64_t batch, int64_t n, int64_
  * Any alignment; the ranges must not overlap (TR_ERR_OVERLAP). */
 tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream);
 
+/* Transposed operand tiles: the shared-memory load stage of the padded SGEMM
+ * of "Padded Shared Memory: Eliminating Bank Conflicts" on its own.  Each
+ * BM x BK tile of the row-major M x K fp32 matrix `a` (row pitch lda) is
+ * staged transposed in shared memory with a row pitch of BM + pad words and
+ * written, unpadded, to `out`: tile (mt, kt) at out + (mt*(K/BK) + kt)*BK*BM,
+ * element (k, m) at k*BM + m, i.e. out holds A[mt*BM + m][kt*BK + k].
+ * BM in {64, 128}, BK in {8, 16, 32}, pad in 0..8 or negative for the page's
+ * rule (32 / BK) % 8.  M and K must be multiples of BM and BK, `a` 16-byte
+ * aligned and lda a multiple of 4 (float4 loads), else TR_ERR_UNSUPPORTED;
+ * `out` (M*K words) must not overlap `a` (TR_ERR_OVERLAP).  Device pointers,
+ * caller-owned; asynchronous on `stream`. */
+tr_status tr_operand_tiles_f32(const float *a, float *out, int64_t m, int64_t k, int64_t lda,
+                               int32_t bm, int32_t bk, int32_t pad, tr_stream_t stream);
+
+/* Column-read microbenchmark of a 32 x 32 shared tile of 4-byte words
+ * ("Shared-memory tiling and bank conflicts", "Expose a shared-memory bank
+ * conflict").  `blocks` blocks of 256 threads each fill one tile holding value
+ * row*32 + col at logical (row, col) in the chosen layout, then lane l of warp
+ * w reads logical (l, (r + w) % 32) for r < reps and folds the values
+ * (acc = rotl(acc, 1) ^ value, starting from 0):
+ *   layout 0: row pitch 32 (a column read is a 32-way bank conflict)
+ *   layout 1: row pitch 33 (the padded tile, conflict-free)
+ *   layout 2: pitch 32 with column index XOR row (swizzled, conflict-free)
+ *   layout 3: pitch 32 read along rows, logical ((r + w) % 32, l) (reference)
+ * `result` (device, blocks*256 words, caller-owned) receives each thread's
+ * fold, so the reads cannot be optimised away and the run is checkable.
+ * Time it with events on `stream` to compare layouts. */
+tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *result,
+                        tr_stream_t stream);
+
 /* Host-only planning: the variant tr_transpose_ex would run for these
  * arguments and options (a tr_variant value, never AUTO), or a negative
  * tr_status on invalid arguments.  Makes no CUDA call. */

@@ -90,6 +90,9 @@ SIGNATURES = {
     "tr_transpose_inplace_f32": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_transpose_inplace_bf16": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_plan_variant": ([ctypes.POINTER(Args), ctypes.POINTER(Options)], ctypes.c_int32),
+    "tr_bank_probe": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, VP, VP], ctypes.c_int),
+    "tr_operand_tiles_f32": ([VP, VP, I64, I64, I64, ctypes.c_int32, ctypes.c_int32,
+                              ctypes.c_int32, VP], ctypes.c_int),
     "tr_device_status": ([], ctypes.c_int),
     "tr_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tr_last_error": ([], ctypes.c_char_p),
@@ -175,6 +178,14 @@ def tr_copy(in_ptr, out_ptr, nbytes, stream=0) -> int:
 
 def tr_plan_variant(args: Args, opts: Options | None = None) -> int:
     return _call("tr_plan_variant", ctypes.byref(args), ctypes.byref(opts) if opts else None)
+
+
+def tr_operand_tiles_f32(a_ptr, out_ptr, m, k, lda, bm, bk, pad=-1, stream=0) -> int:
+    return _call("tr_operand_tiles_f32", a_ptr, out_ptr, m, k, lda, bm, bk, pad, stream)
+
+
+def tr_bank_probe(layout, reps, blocks, result_ptr, stream=0) -> int:
+    return _call("tr_bank_probe", layout, reps, blocks, result_ptr, stream)
 
 
 def tr_device_status() -> int:

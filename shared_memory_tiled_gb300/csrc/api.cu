@@ -306,6 +306,49 @@ tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream) {
     return TR_OK;
 }
 
+tr_status tr_operand_tiles_f32(const float *a, float *out, int64_t m, int64_t k, int64_t lda,
+                               int32_t bm, int32_t bk, int32_t pad, tr_stream_t stream) {
+    if (m < 0 || k < 0) return TR_ERR_BAD_DIM;
+    const bool shape_ok = (bm == 64 || bm == 128) && (bk == 8 || bk == 16 || bk == 32);
+    if (!shape_ok || pad > 8) return TR_ERR_UNSUPPORTED;
+    if (pad < 0) pad = (32 / bk) % 8;  // the page's padding rule
+    if (m == 0 || k == 0) return TR_OK;
+    if (!a || !out) return TR_ERR_NULL;
+    if (lda < k) return TR_ERR_BAD_LD;
+    if (m % bm || k % bk) return TR_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(a) & 15u) || (lda & 3)) return TR_ERR_UNSUPPORTED;
+    int64_t ext_a, bytes_a, bytes_out;
+    if (!tr::mul_add(m - 1, lda, k, &ext_a) || !tr::mul_add(ext_a, 4, 0, &bytes_a) ||
+        !tr::mul_add(m, k * 4, 0, &bytes_out))
+        return TR_ERR_BAD_DIM;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), o0 = reinterpret_cast<uintptr_t>(out);
+    if (a0 + uintptr_t(bytes_a) < a0 || o0 + uintptr_t(bytes_out) < o0) return TR_ERR_BAD_DIM;
+    if (a0 < o0 + uintptr_t(bytes_out) && o0 < a0 + uintptr_t(bytes_a)) return TR_ERR_OVERLAP;
+    const cudaError_t e = tr::launch_operand_tiles(
+        reinterpret_cast<const uint32_t *>(a), reinterpret_cast<uint32_t *>(out), m, k, lda, bm, bk,
+        pad, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tr::set_error("operand tile launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
+tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *result,
+                        tr_stream_t stream) {
+    if (layout < 0 || layout > 3) return TR_ERR_UNSUPPORTED;
+    if (reps < 0 || blocks < 0) return TR_ERR_BAD_DIM;
+    if (blocks == 0) return TR_OK;
+    if (!result) return TR_ERR_NULL;
+    const cudaError_t e = tr::launch_bank_probe(layout, reps, blocks, result,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tr::set_error("bank probe launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
 int32_t tr_plan_variant(const tr_args *args, const tr_options *opts) {
     tr::Problem p{};
     bool empty = false;

@@ -55,6 +55,10 @@ cudaError_t launch_tile_vec(const Problem &p, bool vec_in, bool vec_out, const V
 // `why` receives a static message for non-CUDA failures.
 cudaError_t launch_tma(const Problem &p, const TmaConfig &cfg, const char **why);
 cudaError_t launch_copy(const void *in, void *out, size_t bytes, cudaStream_t stream);
+cudaError_t launch_bank_probe(int layout, int reps, int blocks, uint32_t *result,
+                              cudaStream_t stream);
+cudaError_t launch_operand_tiles(const uint32_t *a, uint32_t *out, int64_t m, int64_t k,
+                                 int64_t lda, int bm, int bk, int pad, cudaStream_t stream);
 cudaError_t launch_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
                            int64_t stride, cudaStream_t stream);
 

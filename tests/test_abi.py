@@ -158,3 +158,25 @@ def test_inplace_argument_errors(lib, fn):
     assert f(FAKE_IN, 2, 4, 4, 15) == B.Status.ERR_BAD_LD
     assert f(FAKE_IN, 1, 1 << 40, 1 << 40, 0) == B.Status.ERR_BAD_DIM
     assert f(0, 0, 4, 4, 16) == B.Status.OK and f(0, 3, 0, 0, 0) == B.Status.OK
+
+
+def test_operand_tiles_argument_errors(lib):
+    f = B.tr_operand_tiles_f32
+    assert f(FAKE_IN, FAKE_OUT, -1, 16, 16, 128, 16) == B.Status.ERR_BAD_DIM
+    assert f(FAKE_IN, FAKE_OUT, 128, 16, 16, 96, 16) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT, 128, 16, 16, 128, 12) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT, 128, 16, 16, 128, 16, 9) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT, 100, 16, 16, 128, 16) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN + 4, FAKE_OUT, 128, 16, 16, 128, 16) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT, 128, 16, 18, 128, 16) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT, 128, 16, 8, 128, 16) == B.Status.ERR_BAD_LD
+    assert f(0, FAKE_OUT, 128, 16, 16, 128, 16) == B.Status.ERR_NULL
+    assert f(FAKE_IN, FAKE_IN + 64, 128, 16, 16, 128, 16) == B.Status.ERR_OVERLAP
+    assert f(0, 0, 0, 16, 16, 128, 16) == B.Status.OK
+
+
+def test_bank_probe_argument_errors(lib):
+    assert B.tr_bank_probe(4, 1, 1, FAKE_OUT) == B.Status.ERR_UNSUPPORTED
+    assert B.tr_bank_probe(0, -1, 1, FAKE_OUT) == B.Status.ERR_BAD_DIM
+    assert B.tr_bank_probe(0, 1, 1, 0) == B.Status.ERR_NULL
+    assert B.tr_bank_probe(0, 1, 0, 0) == B.Status.OK
