@@ -58,6 +58,7 @@ def read_peaks():
 KERNEL_SOURCES = {
     "k_tile_vec": ["tile_vec.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h"],
     "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
+    "k_tma_warp": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
     "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_copy_aligned": ["copy.cu", "tr_internal.h"],
@@ -386,8 +387,9 @@ def run_ours(args):
         raise SystemExit("bench: end-to-end output differs from the transposed input")
 
     peak, peak_kind = read_peaks()
-    kname = {B.Variant.TMA: "k_tma", B.Variant.TILE_VEC: "k_tile_vec",
-             B.Variant.TILE_PAD: "k_tile_pad"}.get(planned, str(planned.name).lower())
+    kname = {B.Variant.TMA: "k_tma" if args.schedule == 1 else "k_tma_warp",
+             B.Variant.TILE_VEC: "k_tile_vec", B.Variant.TILE_PAD: "k_tile_pad",
+             B.Variant.NAIVE_ROW: "k_naive", B.Variant.NAIVE_COL: "k_naive"}.get(planned, "?")
     if inplace:
         kname = "k_inplace"
     traffic, traffic_note = recorded_traffic(kname, w.name)
