@@ -97,7 +97,9 @@ typedef enum tr_variant {
  * TILE_VEC tile shapes (rows x cols, elements) with 256 threads: fp32 64x64
  * (default), 128x64, 64x128, 128x128; bf16 128x128 (default), 256x128,
  * 128x256.  With 128 threads: fp32 64x64, 32x64, 128x64; bf16 128x128,
- * 64x128.  Other combinations return TR_ERR_UNSUPPORTED. */
+ * 64x128.  With 64 threads: fp32 32x64, 64x32; bf16 64x128, 128x64.  With 32
+ * threads (one warp, so the tile barrier is a warp barrier): fp32 32x32,
+ * bf16 64x64.  Other combinations return TR_ERR_UNSUPPORTED. */
 typedef struct tr_options {
     int32_t variant;      /* tr_variant                                                  */
     int32_t pad;          /* TILE_PAD: shared row pitch is 32 + pad elements, 0..8        */
@@ -112,7 +114,7 @@ typedef struct tr_options {
                            * TMA: 0 = default, 1 = one pipeline per block (64x64 fp32 /
                            *   128x128 bf16 tiles, one block barrier per tile),
                            *   2 = one pipeline per warp (32x32 fp32 / 64x64 bf16 tiles) */
-    int32_t threads;      /* TILE_VEC: threads per block, 128 or 256, 0 = default        */
+    int32_t threads;      /* TILE_VEC: threads per block, 32, 64, 128 or 256, 0 = default */
 } tr_options;
 
 /* Full argument set of one (possibly batched) transpose; see the conventions

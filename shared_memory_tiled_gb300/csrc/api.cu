@@ -97,7 +97,9 @@ bool options_valid(const tr_options *o) {
     if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
         return false;
     if (o->schedule < 0 || o->schedule > 2) return false;
-    if (o->threads != 0 && o->threads != 128 && o->threads != 256) return false;
+    if (o->threads != 0 && o->threads != 32 && o->threads != 64 && o->threads != 128 &&
+        o->threads != 256)
+        return false;
     return true;
 }
 

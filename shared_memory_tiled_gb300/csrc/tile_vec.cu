@@ -288,12 +288,17 @@ cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecC
         if constexpr (sizeof(T) == 4) {
             if (mr == 32 && mc == 16) return launch_shape<T, 32, 16, 128>(p, vec_in, vec_out, diag, pf);
         }
+    } else if (nt == 64) {
+        if (mr == 8 && mc == 16) return launch_shape<T, 8, 16, 64>(p, vec_in, vec_out, diag, pf);
+        if (mr == 16 && mc == 8) return launch_shape<T, 16, 8, 64>(p, vec_in, vec_out, diag, pf);
+    } else if (nt == 32) {
+        if (mr == 8 && mc == 8) return launch_shape<T, 8, 8, 32>(p, vec_in, vec_out, diag, pf);
     }
     *why = sizeof(T) == 4
                ? "vector tile: 256 threads take 64x64, 128x64, 64x128 or 128x128 fp32 tiles; "
-                 "128 threads take 64x64, 32x64 or 128x64"
+                 "128 threads 64x64, 32x64 or 128x64; 64 threads 32x64 or 64x32; 32 threads 32x32"
                : "vector tile: 256 threads take 128x128, 256x128 or 128x256 bf16 tiles; "
-                 "128 threads take 128x128 or 64x128";
+                 "128 threads 128x128 or 64x128; 64 threads 64x128 or 128x64; 32 threads 64x64";
     return cudaErrorInvalidValue;
 }
 

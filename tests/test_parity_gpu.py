@@ -48,6 +48,8 @@ SHAPES = [(1, 1), (1, 300), (300, 1), (64, 64), (128, 128), (200, 333), (257, 12
 
 VEC_SHAPES = {U32: [(128, 64), (64, 128), (128, 128)], U16: [(256, 128), (128, 256)]}
 VEC_128 = {U32: [(64, 64), (32, 64), (128, 64)], U16: [(128, 128), (64, 128)]}
+VEC_SMALL = {U32: [(64, 32, 64), (64, 64, 32), (32, 32, 32)],
+             U16: [(64, 64, 128), (64, 128, 64), (32, 64, 64)]}  # threads, rows, cols
 
 
 def _variants(dtype, aligned):
@@ -56,6 +58,8 @@ def _variants(dtype, aligned):
           dict(variant=V.TILE_PAD, pad=2), dict(variant=V.TILE_VEC), dict(variant=V.AUTO)]
     vs += [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]]
     vs += [dict(variant=V.TILE_VEC, threads=128, tile_rows=r, tile_cols=c) for r, c in VEC_128[dtype]]
+    vs += [dict(variant=V.TILE_VEC, threads=n, tile_rows=r, tile_cols=c)
+           for n, r, c in VEC_SMALL[dtype]]
     vs += [dict(variant=V.TILE_VEC, schedule=2),
            dict(variant=V.TILE_VEC, schedule=2, tile_rows=VEC_SHAPES[dtype][0][0],
                 tile_cols=VEC_SHAPES[dtype][0][1])]
@@ -200,6 +204,8 @@ def test_workload_full_size(name):
             for r, c in VEC_SHAPES[U32 if es == 4 else U16]]
     kws += [dict(variant=V.TILE_VEC, threads=128, tile_rows=r, tile_cols=c)
             for r, c in VEC_128[U32 if es == 4 else U16]]
+    kws += [dict(variant=V.TILE_VEC, threads=n, tile_rows=r, tile_cols=c)
+            for n, r, c in VEC_SMALL[U32 if es == 4 else U16]]
     if aligned:
         kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1)]
     if name.startswith("c1"):
