@@ -25,7 +25,9 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["api.cu", "copy.cu", "tile_lsu.cu", "tile_vec.cu", "tile_tma.cu", "inplace.cu", "bank_probe.cu", "operand_tiles.cu"]
+SOURCES = ["api.cu", "copy.cu", "tile_lsu.cu", "tile_vec.cu", "tile_vec_u32.cu",
+           "tile_vec_u32_prefetch.cu", "tile_vec_u16.cu", "tile_vec_u16_prefetch.cu",
+           "tile_tma.cu", "inplace.cu", "bank_probe.cu", "operand_tiles.cu"]
 
 
 def nvcc() -> str:
@@ -57,7 +59,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), max(2, os.cpu_count() or 2))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]

@@ -1,0 +1,302 @@
+// Vectorised swizzled tile transpose (kernel template and per-shape launch;
+// the instantiations are spread over tile_vec_*.cu to compile in parallel):
+// 16-byte global loads and stores, a
+// shared tile read and written with 16-byte accesses in an XOR-swizzled layout,
+// and a register micro-transpose.
+//
+// A 16-byte chunk holds V = 16 / sizeof(T) elements (4 fp32 or 8 bf16).  The
+// block (NT = 128 or 256 threads) stages a TR x TC tile, TR = V*MR rows and TC = V*MC
+// columns: MR x MC micro-blocks of V x V elements, e.g. 64x64 fp32 (16 KiB) or
+// 128x128 bf16 (32 KiB) for MR = MC = 16.
+//
+// Phase 1 (load): thread t takes chunk cc = t % MC of tile rows t / MC + k*NT/MC,
+//   with 16-byte global loads (a warp reads whole MC*16-byte row segments), all
+//   of them in flight before the first shared store.
+// Shared layout: chunk cc of tile row r is stored at chunk position
+//   cc ^ ((r / V) % 8) of that row.  A 16-byte shared access is served in
+//   phases of 8 lanes; it is conflict-free when the 8 lanes hit 8 distinct
+//   positions modulo 8 (each 128 bytes of a row spans all 32 banks once).
+//   Phase-1 stores: 8 lanes = 8 consecutive chunks of one row -> distinct.
+// Phase 2 (transpose): micro-block u = t + NT*j has A = u % MR, C = u / MR and
+//   covers tile rows V*A..V*A+V-1 of chunk C.  Its V shared reads (rows V*A+m,
+//   chunk C) land at positions C ^ (A % 8); the 8 lanes of a phase have 8
+//   consecutive A and one C -> distinct.  The register transpose (renaming
+//   for fp32, 32 byte permutes for bf16) gives V output rows V*C+m', each with
+//   one chunk at output columns V*A..: consecutive lanes write consecutive
+//   chunks, MR*16 contiguous bytes of an output row.
+//
+// This is the padded tile of "Shared memory and the bank conflict" (sections
+// "Turn the tile around on chip" and "Banks") moved to 16-byte accesses: the
+// +1 padding that spreads a 4-byte column walk over the banks cannot keep
+// 16-byte rows aligned, so the spreading is done by the XOR swizzle instead
+// ("Shared-memory tiling and bank conflicts": pad or swizzle tiles when column
+// access creates bank conflicts).
+//
+// Misaligned sides.  VEC_IN = false loads single elements (any pitch).  With
+// SHIFT_OUT the output rows need not start on 16-byte boundaries (e.g. a row
+// pitch of 12289 fp32): for each output row the block finds the number d of
+// elements before the row's first 16-byte boundary inside the tile, and lane A
+// stores the aligned chunk made of its own last V-d elements and the first d
+// of lane A+1 (fetched with a warp shuffle); the d head elements and the V-d
+// tail elements of the tile's row segment go out as single elements.  Partial
+// tiles at the matrix edge always use bounds-checked element accesses except
+// where a whole chunk is in range on an aligned side.
+#pragma once
+
+#include "tile_geom.cuh"
+#include "tr_internal.h"
+#include "vec_common.cuh"
+
+#include <mutex>
+
+namespace tr {
+namespace vec {
+
+// Elements d .. d+V-1 of the 2V-element sequence (own, next), 0 < d < V.
+template <typename T>
+__device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int d) {
+    uint32_t e[8] = {own.w[0], own.w[1], own.w[2], own.w[3],
+                     next.w[0], next.w[1], next.w[2], next.w[3]};
+    const int words = sizeof(T) == 4 ? d : d >> 1;  // whole-word part of the shift
+    if (words & 2) {
+#pragma unroll
+        for (int k = 0; k < 6; ++k) e[k] = e[k + 2];
+    }
+    if (words & 1) {
+#pragma unroll
+        for (int k = 0; k < 5; ++k) e[k] = e[k + 1];
+    }
+    if (sizeof(T) == 2 && (d & 1)) {
+        // odd 16-bit shift: high half of word k, low half of word k+1
+#pragma unroll
+        for (int k = 0; k < 4; ++k) e[k] = __byte_perm(e[k], e[k + 1], 0x5432);
+    }
+    return make_uint4(e[0], e[1], e[2], e[3]);
+}
+
+template <typename T, int MR, int MC, int NT, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
+__global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
+                                                 Geometry g, bool diagonal) {
+    constexpr int V = VecTraits<T>::V;
+    constexpr int TR = V * MR, TC = V * MC;  // tile rows / columns in elements
+    constexpr int MB = MR * MC / NT;         // micro-blocks per thread
+    constexpr int RPP = NT / MC;             // tile rows per load pass
+    constexpr int LOADS = TR / RPP;          // chunks each thread loads
+    static_assert(MR >= 8 && MR <= 32 && MC >= 8 && NT % MC == 0 && (MR * MC) % NT == 0,
+                  "unsupported tile shape");
+    extern __shared__ uint4 smem[];          // TR rows of MC chunks
+
+    const int t = threadIdx.x;
+    const int lcc = t % MC, lr = t / MC;
+
+    // Phase 1a: this thread's chunks of tile `tile`, global -> registers, all
+    // loads issued before any is used.
+    Chunk ld[LOADS];
+    auto load_tile = [&](int64_t tile) {
+        int64_t b, tr, tc;
+        split_tile(g, tile, diagonal, b, tr, tc);
+        const T *src = in + b * g.stride_in;
+        const int64_t r0 = tr * TR, c0 = tc * TC;
+        const bool full = (r0 + TR <= g.rows) && (c0 + TC <= g.cols);
+        const int64_t gc = c0 + lcc * V;
+        if (full && VEC_IN) {
+#pragma unroll
+            for (int k = 0; k < LOADS; ++k)
+                ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + (r0 + lr + RPP * k) * g.ld_in + gc));
+        } else {
+#pragma unroll
+            for (int k = 0; k < LOADS; ++k) {
+                const int64_t gr = r0 + lr + RPP * k;
+                if (VEC_IN && gr < g.rows && gc + V <= g.cols) {
+                    ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + gc));
+                } else {
+                    T e[V];
+#pragma unroll
+                    for (int q = 0; q < V; ++q)
+                        e[q] = (gr < g.rows && gc + q < g.cols) ? src[gr * g.ld_in + gc + q] : T(0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (sizeof(T) == 4)
+                            ld[k].w[q] = uint32_t(e[q]);
+                        else
+                            ld[k].w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                    }
+                }
+            }
+        }
+    };
+
+    // With PREFETCH the grid is persistent and the loads of a block's next
+    // tile are issued as soon as the current tile sits in shared memory, so
+    // they are in flight while the current tile is transposed and stored
+    // ("Shared-memory tiling and bank conflicts", "Protect tile phases": one
+    // stage loads future data while another is consumed).  The registers are
+    // the second buffer; the shared tile is reused once every thread passed
+    // the barrier that ends the previous tile's reads.
+    if (PREFETCH && blockIdx.x < g.total) load_tile(blockIdx.x);
+
+    for (int64_t tile = blockIdx.x; tile < g.total; tile += gridDim.x) {
+        int64_t b, tr, tc;
+        split_tile(g, tile, diagonal, b, tr, tc);
+        T *dst = out + b * g.stride_out;
+        const int64_t r0 = tr * TR, c0 = tc * TC;
+        const bool full = (r0 + TR <= g.rows) && (c0 + TC <= g.cols);
+
+        if (!PREFETCH) load_tile(tile);
+        if (tile != blockIdx.x) __syncthreads();  // previous tile fully read
+        // Phase 1b: registers -> swizzled shared tile.
+#pragma unroll
+        for (int k = 0; k < LOADS; ++k) {
+            const int r = lr + RPP * k;
+            smem[r * MC + (lcc ^ ((r / V) & 7))] = ld[k].v;
+        }
+        __syncthreads();
+        if (PREFETCH && tile + gridDim.x < g.total) load_tile(tile + gridDim.x);
+
+        // ---- phase 2: micro-blocks -> registers -> transpose -> global
+#pragma unroll
+        for (int j = 0; j < MB; ++j) {
+            const int u = t + NT * j;
+            const int A = u % MR, C = u / MR;
+            Chunk x[V], y[V];
+#pragma unroll
+            for (int m = 0; m < V; ++m) x[m].v = smem[(V * A + m) * MC + (C ^ (A & 7))];
+            micro_transpose(x, y);
+            const int64_t oc = r0 + V * A;  // first output column of this lane's chunk
+            if (full && !SHIFT_OUT) {
+#pragma unroll
+                for (int m = 0; m < V; ++m)
+                    __stcs(reinterpret_cast<uint4 *>(dst + (c0 + V * C + m) * g.ld_out + oc), y[m].v);
+            } else if (full) {
+#pragma unroll
+                for (int m = 0; m < V; ++m) {
+                    T *row = dst + (c0 + V * C + m) * g.ld_out;
+                    Chunk nb;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) nb.w[k] = __shfl_down_sync(0xffffffffu, y[m].w[k], 1);
+                    const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
+                    const int d = (V - s) % V;  // elements before the first 16-byte boundary
+                    if (d == 0) {
+                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                    } else {
+                        if (A < MR - 1)
+                            __stcs(reinterpret_cast<uint4 *>(row + oc + d), window<T>(y[m], nb, d));
+                        if (A == 0) {
+#pragma unroll
+                            for (int q = 0; q < V; ++q)
+                                if (q < d) row[oc + q] = elem<T>(y[m], q);
+                        } else if (A == MR - 1) {
+#pragma unroll
+                            for (int q = 0; q < V; ++q)
+                                if (q >= d) row[oc + q] = elem<T>(y[m], q);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < V; ++m) {
+                    const int64_t orow = c0 + V * C + m;
+                    if (orow >= g.cols) break;
+                    T *row = dst + orow * g.ld_out;
+                    if (!SHIFT_OUT && oc + V <= g.rows) {
+                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            if (oc + q < g.rows) row[oc + q] = elem<T>(y[m], q);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Shared memory of one instantiation; above 48 KiB it needs an opt-in, done
+// once per device.
+// One instantiation's launch.  Above 48 KiB of shared memory the kernel needs
+// an opt-in, and a persistent grid needs the number of resident blocks per
+// SM: both are found once per device and cached.
+template <typename T, int MR, int MC, int NT, bool VI, bool SO, bool PF>
+cudaError_t launch_one(const Problem &p, bool diagonal) {
+    constexpr int V = VecTraits<T>::V;
+    constexpr size_t smem = size_t(V * MR) * MC * 16;
+    auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
+    static int resident[64] = {};  // 0 = not set up on that device yet
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!resident[dev]) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!resident[dev]) {
+            if (smem > 48 * 1024) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                if (e != cudaSuccess) return e;
+            }
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, smem);
+            if (e != cudaSuccess) return e;
+            resident[dev] = n > 0 ? n : 1;
+        }
+    }
+    const Geometry g = make_geometry(p, V * MR, V * MC);
+    int64_t grid = g.total;
+    if (PF) {
+        const int64_t cap = int64_t(sm_count()) * resident[dev];
+        if (grid > cap) grid = cap;
+    }
+    kern<<<grid_blocks(grid), NT, smem, p.stream>>>(static_cast<const T *>(p.in),
+                                                     static_cast<T *>(p.out), g, diagonal);
+    return cudaGetLastError();
+}
+
+template <typename T, int MR, int MC, int NT, bool PF>
+cudaError_t launch_align(const Problem &p, bool vec_in, bool vec_out, bool diagonal) {
+    if (vec_in && vec_out) return launch_one<T, MR, MC, NT, true, false, PF>(p, diagonal);
+    if (vec_in) return launch_one<T, MR, MC, NT, true, true, PF>(p, diagonal);
+    if (vec_out) return launch_one<T, MR, MC, NT, false, false, PF>(p, diagonal);
+    return launch_one<T, MR, MC, NT, false, true, PF>(p, diagonal);
+}
+
+// Supported shapes (micro-blocks MR x MC, threads NT).  256 threads for every
+// shape; 128 threads for the smaller tiles, which doubles the loads each
+// thread keeps in flight and lets more blocks share an SM.
+template <typename T, bool PF>
+cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecConfig &cfg,
+                         const char **why) {
+    constexpr int V = VecTraits<T>::V;
+    const bool diag = cfg.tile_order == 1;
+    const int nt = cfg.threads ? cfg.threads : 256;
+    int mr = cfg.tile_rows ? cfg.tile_rows / V : 16;
+    int mc = cfg.tile_cols ? cfg.tile_cols / V : 16;
+    if ((cfg.tile_rows % V) || (cfg.tile_cols % V)) mr = mc = 0;
+    if (nt == 256) {
+        if (mr == 16 && mc == 16) return launch_align<T, 16, 16, 256, PF>(p, vec_in, vec_out, diag);
+        if (mr == 32 && mc == 16) return launch_align<T, 32, 16, 256, PF>(p, vec_in, vec_out, diag);
+        if (mr == 16 && mc == 32) return launch_align<T, 16, 32, 256, PF>(p, vec_in, vec_out, diag);
+        if constexpr (sizeof(T) == 4) {
+            if (mr == 32 && mc == 32) return launch_align<T, 32, 32, 256, PF>(p, vec_in, vec_out, diag);
+        }
+    } else if (nt == 128) {
+        if (mr == 16 && mc == 16) return launch_align<T, 16, 16, 128, PF>(p, vec_in, vec_out, diag);
+        if (mr == 8 && mc == 16) return launch_align<T, 8, 16, 128, PF>(p, vec_in, vec_out, diag);
+        if constexpr (sizeof(T) == 4) {
+            if (mr == 32 && mc == 16) return launch_align<T, 32, 16, 128, PF>(p, vec_in, vec_out, diag);
+        }
+    } else if (nt == 64) {
+        if (mr == 8 && mc == 16) return launch_align<T, 8, 16, 64, PF>(p, vec_in, vec_out, diag);
+        if (mr == 16 && mc == 8) return launch_align<T, 16, 8, 64, PF>(p, vec_in, vec_out, diag);
+    } else if (nt == 32) {
+        if (mr == 8 && mc == 8) return launch_align<T, 8, 8, 32, PF>(p, vec_in, vec_out, diag);
+    }
+    *why = sizeof(T) == 4
+               ? "vector tile: 256 threads take 64x64, 128x64, 64x128 or 128x128 fp32 tiles; "
+                 "128 threads 64x64, 32x64 or 128x64; 64 threads 32x64 or 64x32; 32 threads 32x32"
+               : "vector tile: 256 threads take 128x128, 256x128 or 128x256 bf16 tiles; "
+                 "128 threads 128x128 or 64x128; 64 threads 64x128 or 128x64; 32 threads 64x64";
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vec
+}  // namespace tr

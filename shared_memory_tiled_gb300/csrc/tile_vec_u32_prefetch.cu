@@ -1,0 +1,11 @@
+// Instantiations of the vectorised swizzled tile: fp32 persistent prefetching blocks.
+#include "tile_vec_kernel.cuh"
+
+namespace tr {
+
+cudaError_t launch_vec_u32_prefetch(const Problem &p, bool vec_in, bool vec_out, const VecConfig &cfg,
+                           const char **why) {
+    return vec::launch_typed<uint32_t, true>(p, vec_in, vec_out, cfg, why);
+}
+
+}  // namespace tr
