@@ -113,7 +113,9 @@ typedef struct tr_options {
                            *   2 = persistent blocks that prefetch their next tile;
                            * TMA: 0 = default, 1 = one pipeline per block (64x64 fp32 /
                            *   128x128 bf16 tiles, one block barrier per tile),
-                           *   2 = one pipeline per warp (32x32 fp32 / 64x64 bf16 tiles) */
+                           *   2 = one pipeline per warp (32x32 fp32 / 64x64 bf16 tiles),
+                           *   3 = per-warp TMA loads, register transpose and 16-byte
+                           *       global stores (no output buffer, no TMA store)        */
     int32_t threads;      /* TILE_VEC: threads per block, 32, 64, 128 or 256, 0 = default */
 } tr_options;
 

@@ -4,6 +4,7 @@
 // reported without a GPU.
 #include "tr_internal.h"
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -96,7 +97,7 @@ bool options_valid(const tr_options *o) {
     if (o->out_stages != 0 && (o->out_stages < 2 || o->out_stages > 4)) return false;
     if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
         return false;
-    if (o->schedule < 0 || o->schedule > 2) return false;
+    if (o->schedule < 0 || o->schedule > 3) return false;
     if (o->threads != 0 && o->threads != 32 && o->threads != 64 && o->threads != 128 &&
         o->threads != 256)
         return false;
@@ -145,6 +146,11 @@ tr_status run(const tr_args *a, const tr_options *o) {
         case TR_VARIANT_NAIVE_COL: e = launch_naive(p, false); break;
         case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
         case TR_VARIANT_TILE_VEC: {
+            if (o && o->schedule == 3) {
+                set_error("schedule 3 (TMA loads, register stores) belongs to the TMA variant",
+                          cudaSuccess);
+                return TR_ERR_UNSUPPORTED;
+            }
             VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
                           o && o->schedule == 2, o ? o->threads : 0};
             if (cfg.tile_rows == 0 && cfg.tile_cols == 0)
@@ -234,17 +240,17 @@ tr_status run_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t l
 }  // namespace
 
 int sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // 0 = not queried yet (zero-initialised: static)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
     if (dev < 0 || dev >= 64) dev = 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_acquire);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             n = 1;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_release);
     }
-    return cache[dev];
+    return n;
 }
 
 }  // namespace tr

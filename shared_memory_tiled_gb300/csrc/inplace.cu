@@ -9,7 +9,8 @@
 // reads are in).  A diagonal tile is its own partner.  No other block reads or
 // writes either tile, so blocks never race.
 //
-// Layout and lane mapping are those of the vectorised swizzled tile (tile_vec.cu):
+// Layout and lane mapping are those of the vectorised swizzled tile
+// (tile_vec_kernel.cuh):
 // a 16V x 16V tile (64x64 fp32, 128x128 bf16), chunk cc of tile row r stored at
 // chunk position cc ^ ((r / V) % 8), 256 threads, 16-byte loads and stores and a
 // register micro-transpose; VEC = false moves single elements (any alignment).
@@ -20,6 +21,7 @@
 #include "tr_internal.h"
 #include "vec_common.cuh"
 
+#include <atomic>
 #include <mutex>
 
 namespace tr {
@@ -123,18 +125,18 @@ cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
     constexpr size_t smem = 2 * size_t(16 * V) * 16 * 16;
     auto kern = k_inplace<T, VEC>;
     if (smem > 48 * 1024) {
-        static bool opted[64] = {};
+        static std::atomic<bool> opted[64];  // per device, zero-initialised (static)
         static std::mutex mu;
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!opted[dev]) {
+        if (!opted[dev].load(std::memory_order_acquire)) {
             std::lock_guard<std::mutex> lock(mu);
-            if (!opted[dev]) {
+            if (!opted[dev].load(std::memory_order_relaxed)) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
                 if (e != cudaSuccess) return e;
-                opted[dev] = true;
+                opted[dev].store(true, std::memory_order_release);
             }
         }
     }

@@ -1,6 +1,6 @@
 // Transpose kernels that move one element per access with ordinary loads and
 // stores: the naive one-element-per-thread forms and the 32x32 tile with a
-// padded shared row pitch (the vectorised swizzled tile is in tile_vec.cu).
+// padded shared row pitch (the vectorised swizzled tile is in tile_vec_kernel.cuh).
 //
 // Element words are moved as raw bits: uint32_t for fp32, uint16_t for bf16.
 // All index arithmetic is 64-bit; tiles are walked through a 1-D grid whose

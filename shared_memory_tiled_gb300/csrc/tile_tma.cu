@@ -45,6 +45,7 @@
 #include "ptx.cuh"
 #include "tr_internal.h"
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -392,6 +393,141 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
     }
 }
 
+// ---------------------------------------------------------------------------
+// TMA loads, register stores.  Per-warp pipelines of TMA box loads as above,
+// but no output buffer and no TMA store: each lane turns its micro-blocks
+// around in registers and stores them straight to global memory with 16-byte
+// stores, lanes with consecutive A (same C) writing consecutive chunks of one
+// output row (8 lanes = 128 contiguous bytes).  Only the input side needs the
+// TMA alignment rules; the output side needs 16-byte aligned rows for the
+// vector stores (the launcher checks) and edge tiles use element stores.
+//
+// That lane map reads 8 micro-blocks of one chunk column per phase, which on
+// the 128-byte swizzle (position = chunk ^ (row % 8)) would put 8 lanes on 2
+// positions (fp32) or 1 (bf16).  So lane A reads its V rows in a rotated
+// order, row V*A + ((m + rot) % V) at step m with rot = A / 2 (fp32) or A
+// (bf16), which makes (row % 8) distinct across the 8 lanes at every step; the
+// rotation is undone in registers before the micro-transpose.
+template <int V>
+__device__ __forceinline__ void unrotate(uint4 (&x)[V], int rot) {
+    // x[m] holds row (m + rot) % V; afterwards x[j] holds row j.
+    uint4 t[V];
+#pragma unroll
+    for (int step = 1; step < V; step <<= 1) {
+        if (rot & step) {
+#pragma unroll
+            for (int j = 0; j < V; ++j) t[j] = x[(j - step + V) % V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) x[j] = t[j];
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
+    using L = WarpTile<T>;
+    constexpr int V = L::V;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int S = g.in_stages;
+    uint8_t *in_buf = base + size_t(warp) * S * L::BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + size_t(nwarps) * S * L::BYTES) + warp * S;
+
+    const int A = lane & 7;
+    const int rot = V == 4 ? (A >> 1) : A;
+    uint32_t roff[2][V];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int C = 4 * p + (lane >> 3);
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+            const int r = V * A + ((m + rot) & (V - 1));
+            roff[p][m] = r * 128 + ((C ^ (r & 7)) << 4);
+        }
+    }
+
+    const int64_t gw = int64_t(blockIdx.x) * nwarps + warp;
+    const int64_t G = int64_t(gridDim.x) * nwarps;
+    const int64_t n_local = gw < g.total ? (g.total - 1 - gw) / G + 1 : 0;
+
+    auto issue_load = [&](int64_t k, int slot) {
+        int32_t b, tr, tc;
+        tile_coords(g, gw + k * G, b, tr, tc);
+        ptx::mbar_arrive_expect_tx(full + slot, L::BYTES);
+        ptx::tma_load_3d(in_buf + size_t(slot) * L::BYTES, &tm_in, full + slot, tc * L::TILE,
+                         tr * L::TILE, b);
+    };
+
+    if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_in);
+        for (int i = 0; i < S; ++i) ptx::mbar_init(full + i, 1);
+        ptx::fence_barrier_init();
+        for (int64_t k = 0; k < n_local && k < S; ++k) issue_load(k, int(k));
+    }
+    __syncwarp();
+
+    int64_t k = 0;
+    bool aborted = false;
+    for (; k < n_local; ++k) {
+        const int slot = int(k % S);
+        const bool ok = ptx::mbar_wait_bounded(full + slot, uint32_t((k / S) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            aborted = true;
+            break;
+        }
+        int32_t b, tr, tc;
+        tile_coords(g, gw + k * G, b, tr, tc);
+        const uint8_t *ib = in_buf + size_t(slot) * L::BYTES;
+        uint4 x[2][V];
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int m = 0; m < V; ++m) x[p][m] = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
+        __syncwarp();  // the slot is read: it may be refilled
+        if (lane == 0 && k + S < n_local) issue_load(k + S, slot);
+
+        T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
+        const int64_t r0 = int64_t(tr) * L::TILE, c0 = int64_t(tc) * L::TILE;
+        const bool full_tile = r0 + L::TILE <= g.rows && c0 + L::TILE <= g.cols;
+        const int64_t oc = r0 + V * A;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int C = 4 * p + (lane >> 3);
+            unrotate<V>(x[p], rot);
+            uint4 y[V];
+            micro_transpose(x[p], y);
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                const int64_t orow = c0 + V * C + m;
+                T *row = dst + orow * g.ld_out;
+                if (full_tile) {
+                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                } else if (orow < g.cols) {
+                    if (oc + V <= g.rows) {
+                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                    } else {
+                        const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
+#pragma unroll
+                        for (int e = 0; e < V; ++e)
+                            if (oc + e < g.rows) {
+                                const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
+                                row[oc + e] = T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
+                            }
+                    }
+                }
+            }
+        }
+    }
+    if (lane == 0 && aborted) {
+        atomicExch(&g_fault_flag, 1u);
+        for (int64_t kk = k; kk < n_local && kk < k + S; ++kk)
+            ptx::mbar_wait_bounded(full + int(kk % S), uint32_t((kk / S) & 1));
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -431,17 +567,19 @@ bool encode_3d(CUtensorMap *map, const void *base, int esize, int64_t elems, int
 
 // Per-device facts and per-configuration occupancy, computed once: the
 // launch path then makes no attribute or occupancy query per call.
+enum Kind { kPerBlock = 0, kPerWarp = 1, kLoadOnly = 2 };
+
 struct DeviceInfo {
-    bool ok = false;
+    std::atomic<bool> ok{false};  // set last, after the fields below are filled
     cudaError_t err = cudaSuccess;
     int sms = 0;
     int max_smem_optin = 0;
-    // [per-warp kernel][esize == 4][in_stages][out_stages]; 0 = not computed
-    int fit[2][2][9][kMaxOutStages + 1] = {};
+    // [kind][esize == 4][in_stages][out_stages]; 0 = not computed
+    std::atomic<int> fit[3][2][9][kMaxOutStages + 1] = {};
 };
 
 constexpr int kMaxDevices = 64;
-constexpr int kWarpsPerBlock = 1;  // per-warp pipeline: one warp per block
+constexpr int kWarpsPerBlock = 1;  // per-warp pipelines: one warp per block
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
@@ -450,34 +588,36 @@ DeviceInfo &device_info() {
     int d = 0;
     cudaError_t e = cudaGetDevice(&d);
     if (e != cudaSuccess || d < 0 || d >= kMaxDevices) {
-        failed.ok = false;
+        failed.ok.store(false);
         failed.err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
         return failed;
     }
     DeviceInfo &info = g_dev[d];
-    if (!info.ok) {
+    if (!info.ok.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_dev_mu);
-        if (!info.ok) {
+        if (!info.ok.load(std::memory_order_relaxed)) {
             int sms = 0, optin = 0;
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
             if (e == cudaSuccess)
                 e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
             // Opt the kernels in to the largest dynamic shared memory once.
-            const void *kernels[4] = {reinterpret_cast<const void *>(k_tma<uint32_t>),
+            const void *kernels[6] = {reinterpret_cast<const void *>(k_tma<uint32_t>),
                                       reinterpret_cast<const void *>(k_tma<uint16_t>),
                                       reinterpret_cast<const void *>(k_tma_warp<uint32_t>),
-                                      reinterpret_cast<const void *>(k_tma_warp<uint16_t>)};
+                                      reinterpret_cast<const void *>(k_tma_warp<uint16_t>),
+                                      reinterpret_cast<const void *>(k_tma_ldst<uint32_t>),
+                                      reinterpret_cast<const void *>(k_tma_ldst<uint16_t>)};
             for (const void *k : kernels)
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
             if (e != cudaSuccess) {
-                failed.ok = false;
+                failed.ok.store(false);
                 failed.err = e;
                 return failed;
             }
             info.sms = sms;
             info.max_smem_optin = optin;
-            info.ok = true;
+            info.ok.store(true, std::memory_order_release);
         }
     }
     return info;
@@ -486,44 +626,60 @@ DeviceInfo &device_info() {
 // Dynamic shared memory: 1 KiB of slack to align the buffers to the 128-byte
 // swizzle's 1 KiB pattern, the tile buffers, one 8-byte mbarrier per input slot.
 template <typename T>
-size_t smem_bytes(bool per_warp, int in_stages, int out_stages) {
-    if (per_warp)
-        return 1024 + size_t(kWarpsPerBlock) *
-                          (size_t(in_stages + out_stages) * WarpTile<T>::BYTES + size_t(in_stages) * 8);
-    return 1024 + size_t(in_stages + out_stages) * TmaTile<T>::BUF_BYTES + size_t(in_stages) * 8;
+size_t smem_bytes(Kind kind, int in_stages, int out_stages) {
+    switch (kind) {
+        case kPerBlock:
+            return 1024 + size_t(in_stages + out_stages) * TmaTile<T>::BUF_BYTES +
+                   size_t(in_stages) * 8;
+        case kPerWarp:
+            return 1024 + size_t(kWarpsPerBlock) * (size_t(in_stages + out_stages) *
+                                                        WarpTile<T>::BYTES + size_t(in_stages) * 8);
+        default:
+            return 1024 + size_t(kWarpsPerBlock) *
+                              (size_t(in_stages) * WarpTile<T>::BYTES + size_t(in_stages) * 8);
+    }
 }
 
 template <typename T>
-int resident_ctas(DeviceInfo &dev, bool per_warp, int in_stages, int out_stages) {
-    int &slot = dev.fit[per_warp][sizeof(T) == 4][in_stages][out_stages];
-    if (slot == 0) {
+int resident_ctas(DeviceInfo &dev, Kind kind, int in_stages, int out_stages) {
+    std::atomic<int> &slot = dev.fit[kind][sizeof(T) == 4][in_stages][out_stages];
+    int cached = slot.load(std::memory_order_acquire);
+    if (cached == 0) {
         int fit = 0;
-        const size_t smem = smem_bytes<T>(per_warp, in_stages, out_stages);
-        const cudaError_t e =
-            per_warp ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_warp<T>,
-                                                                     32 * kWarpsPerBlock, smem)
-                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma<T>, kThreads, smem);
-        slot = (e != cudaSuccess || fit < 1) ? -1 : fit;
+        const size_t smem = smem_bytes<T>(kind, in_stages, out_stages);
+        cudaError_t e;
+        if (kind == kPerBlock)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma<T>, kThreads, smem);
+        else if (kind == kPerWarp)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_warp<T>,
+                                                              32 * kWarpsPerBlock, smem);
+        else
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_ldst<T>,
+                                                              32 * kWarpsPerBlock, smem);
+        cached = (e != cudaSuccess || fit < 1) ? -1 : fit;
+        slot.store(cached, std::memory_order_release);
     }
-    return slot;
+    return cached;
 }
 
 // Defaults, the best measured on GB300: per-warp pipeline with 6 box loads
 // in flight and 2 output buffers (fp32, 4 KiB boxes) or 4 loads and 3 output
-// buffers (bf16, 8 KiB boxes); CTA-wide pipeline with 2 + 2.
-int default_in_stages(size_t esize, bool per_warp) {
-    if (per_warp) return esize == 4 ? 6 : 4;
+// buffers (bf16, 8 KiB boxes); CTA-wide pipeline with 2 + 2; load-only
+// pipeline with 8 (fp32) or 6 (bf16) loads in flight.
+int default_in_stages(size_t esize, Kind kind) {
+    if (kind == kPerWarp) return esize == 4 ? 6 : 4;
+    if (kind == kLoadOnly) return esize == 4 ? 8 : 6;
     return 2;
 }
-int default_out_stages(size_t esize, bool per_warp) {
-    return (per_warp && esize == 2) ? 3 : 2;
+int default_out_stages(size_t esize, Kind kind) {
+    return (kind == kPerWarp && esize == 2) ? 3 : 2;
 }
 
 template <typename T>
 cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **why) {
-    const bool per_warp = cfg.schedule != 1;
-    const int tile = per_warp ? WarpTile<T>::TILE : TmaTile<T>::TILE;
-    const int boxc = TmaTile<T>::BOXC;  // 128-byte box rows either way
+    const Kind kind = cfg.schedule == 1 ? kPerBlock : cfg.schedule == 3 ? kLoadOnly : kPerWarp;
+    const int tile = kind == kPerBlock ? TmaTile<T>::TILE : WarpTile<T>::TILE;
+    const int boxc = TmaTile<T>::BOXC;  // 128-byte box rows in every kind
     const int64_t two31 = int64_t(1) << 31, two40 = int64_t(1) << 40;
     if (p.rows >= two31 || p.cols >= two31 || p.batch >= two31) {
         *why = "TMA coordinates are 32-bit: a dimension is 2^31 or more";
@@ -540,7 +696,8 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     }
     CUtensorMap tm_in, tm_out;
     if (!encode_3d(&tm_in, p.in, p.esize, p.cols, p.rows, p.batch, p.ld_in, sin, boxc, tile) ||
-        !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, boxc, tile)) {
+        (kind != kLoadOnly &&
+         !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, boxc, tile))) {
         *why = "cuTensorMapEncodeTiled rejected the tensor maps";
         return cudaErrorInvalidValue;
     }
@@ -556,32 +713,34 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     g.ld_out = p.ld_out;
     g.stride_out = sout;
     DeviceInfo &dev = device_info();
-    if (!dev.ok) return dev.err;
-    const int stages = cfg.stages > 0 ? cfg.stages : default_in_stages(sizeof(T), per_warp);
-    const int out_stages = cfg.out_stages > 0 ? cfg.out_stages : default_out_stages(sizeof(T), per_warp);
+    if (!dev.ok.load(std::memory_order_acquire)) return dev.err;
+    const int stages = cfg.stages > 0 ? cfg.stages : default_in_stages(sizeof(T), kind);
+    const int out_stages = cfg.out_stages > 0 ? cfg.out_stages : default_out_stages(sizeof(T), kind);
     if (stages < 2 || stages > 8 || out_stages < 2 || out_stages > kMaxOutStages) {
         *why = "TMA stage counts out of range";
         return cudaErrorInvalidValue;
     }
     g.in_stages = stages;
     g.out_stages = out_stages;
-    const size_t smem = smem_bytes<T>(per_warp, stages, out_stages);
+    const size_t smem = smem_bytes<T>(kind, stages, out_stages);
     if (smem > size_t(dev.max_smem_optin)) {
         *why = "TMA pipeline does not fit in shared memory; lower the stage count";
         return cudaErrorInvalidValue;
     }
-    const int fit = resident_ctas<T>(dev, per_warp, stages, out_stages);
+    const int fit = resident_ctas<T>(dev, kind, stages, out_stages);
     if (fit < 1) {
         *why = "TMA kernel cannot be resident with this configuration";
         return cudaErrorInvalidValue;
     }
     int per_sm = cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : fit;
     if (per_sm > fit) per_sm = fit;
-    const int64_t units = per_warp ? (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock : g.total;
+    const int64_t units = kind == kPerBlock ? g.total : (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock;
     int64_t grid = int64_t(dev.sms) * per_sm;
     if (grid > units) grid = units;
-    if (per_warp)
+    if (kind == kPerWarp)
         k_tma_warp<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, tm_out, g);
+    else if (kind == kLoadOnly)
+        k_tma_ldst<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, g);
     else
         k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
     return cudaGetLastError();

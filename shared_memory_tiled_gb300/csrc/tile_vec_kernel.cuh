@@ -47,6 +47,7 @@
 #include "tr_internal.h"
 #include "vec_common.cuh"
 
+#include <atomic>
 #include <mutex>
 
 namespace tr {
@@ -221,15 +222,18 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     constexpr size_t smem = size_t(V * MR) * MC * 16;
     auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
-    static int resident[64] = {};  // 0 = not set up on that device yet
+    // Resident blocks per SM on each device; 0 = not set up on that device yet.
+    static std::atomic<int> resident[64];
     static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!resident[dev]) {
+    int fit = resident[dev].load(std::memory_order_acquire);
+    if (!fit) {
         std::lock_guard<std::mutex> lock(mu);
-        if (!resident[dev]) {
+        fit = resident[dev].load(std::memory_order_relaxed);
+        if (!fit) {
             if (smem > 48 * 1024) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
                 if (e != cudaSuccess) return e;
@@ -237,13 +241,14 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
             int n = 0;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, smem);
             if (e != cudaSuccess) return e;
-            resident[dev] = n > 0 ? n : 1;
+            fit = n > 0 ? n : 1;
+            resident[dev].store(fit, std::memory_order_release);
         }
     }
     const Geometry g = make_geometry(p, V * MR, V * MC);
     int64_t grid = g.total;
     if (PF) {
-        const int64_t cap = int64_t(sm_count()) * resident[dev];
+        const int64_t cap = int64_t(sm_count()) * fit;
         if (grid > cap) grid = cap;
     }
     kern<<<grid_blocks(grid), NT, smem, p.stream>>>(static_cast<const T *>(p.in),

@@ -70,7 +70,9 @@ def _variants(dtype, aligned):
                dict(variant=V.TMA, stages=8, tile_order=1),
                dict(variant=V.TMA, schedule=1), dict(variant=V.TMA, schedule=1, stages=3,
                                                      out_stages=3),
-               dict(variant=V.TMA, schedule=1, stages=deep, tile_order=1)]
+               dict(variant=V.TMA, schedule=1, stages=deep, tile_order=1),
+               dict(variant=V.TMA, schedule=3), dict(variant=V.TMA, schedule=3, stages=2),
+               dict(variant=V.TMA, schedule=3, stages=8, tile_order=1)]
     return vs
 
 
@@ -168,7 +170,8 @@ def test_nan_payloads_survive_every_variant():
 
 
 @pytest.mark.parametrize("variant", [dict(variant=V.TILE_PAD, pad=1), dict(variant=V.TILE_VEC),
-                                     dict(variant=V.TMA)], ids=["pad1", "vec", "tma"])
+                                     dict(variant=V.TMA), dict(variant=V.TMA, schedule=3)],
+                         ids=["pad1", "vec", "tma", "tma_ldst"])
 def test_index_check_repeated(variant):
     """The exact index check run many times: a tile read before it was fully
     written fails it ("Shared memory and the bank conflict", "The barrier")."""
@@ -207,7 +210,7 @@ def test_workload_full_size(name):
     kws += [dict(variant=V.TILE_VEC, threads=n, tile_rows=r, tile_cols=c)
             for n, r, c in VEC_SMALL[U32 if es == 4 else U16]]
     if aligned:
-        kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1)]
+        kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1), dict(variant=V.TMA, schedule=3)]
     if name.startswith("c1"):
         kws += [dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
                 dict(variant=V.TILE_PAD, pad=2), dict(variant=V.NAIVE_ROW),
