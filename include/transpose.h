@@ -95,8 +95,8 @@ typedef enum tr_variant {
 
 /* Tuning knobs for tr_transpose_ex.  Zero-initialise for defaults.
  * TILE_VEC tile shapes (rows x cols, elements) with 256 threads: fp32 64x64
- * (default), 128x64, 64x128, 128x128; bf16 128x128 (default), 256x128,
- * 128x256.  With 128 threads: fp32 64x64, 32x64, 128x64; bf16 128x128,
+ * (default), 128x32, 128x64, 64x128, 128x128; bf16 128x128 (default), 256x64,
+ * 256x128, 128x256.  With 128 threads: fp32 64x64, 32x64, 128x64; bf16 128x128,
  * 64x128.  With 64 threads: fp32 32x64, 64x32; bf16 64x128, 128x64.  With 32
  * threads (one warp, so the tile barrier is a warp barrier): fp32 32x32,
  * bf16 64x64.  Other combinations return TR_ERR_UNSUPPORTED. */

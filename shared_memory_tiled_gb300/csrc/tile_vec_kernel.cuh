@@ -278,6 +278,7 @@ cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecC
     if ((cfg.tile_rows % V) || (cfg.tile_cols % V)) mr = mc = 0;
     if (nt == 256) {
         if (mr == 16 && mc == 16) return launch_align<T, 16, 16, 256, PF>(p, vec_in, vec_out, diag);
+        if (mr == 32 && mc == 8) return launch_align<T, 32, 8, 256, PF>(p, vec_in, vec_out, diag);
         if (mr == 32 && mc == 16) return launch_align<T, 32, 16, 256, PF>(p, vec_in, vec_out, diag);
         if (mr == 16 && mc == 32) return launch_align<T, 16, 32, 256, PF>(p, vec_in, vec_out, diag);
         if constexpr (sizeof(T) == 4) {
@@ -296,9 +297,9 @@ cudaError_t launch_typed(const Problem &p, bool vec_in, bool vec_out, const VecC
         if (mr == 8 && mc == 8) return launch_align<T, 8, 8, 32, PF>(p, vec_in, vec_out, diag);
     }
     *why = sizeof(T) == 4
-               ? "vector tile: 256 threads take 64x64, 128x64, 64x128 or 128x128 fp32 tiles; "
+               ? "vector tile: 256 threads take 64x64, 128x32, 128x64, 64x128 or 128x128 fp32 tiles; "
                  "128 threads 64x64, 32x64 or 128x64; 64 threads 32x64 or 64x32; 32 threads 32x32"
-               : "vector tile: 256 threads take 128x128, 256x128 or 128x256 bf16 tiles; "
+               : "vector tile: 256 threads take 128x128, 256x64, 256x128 or 128x256 bf16 tiles; "
                  "128 threads 128x128 or 64x128; 64 threads 64x128 or 128x64; 32 threads 64x64";
     return cudaErrorInvalidValue;
 }

@@ -46,7 +46,8 @@ SHAPES = [(1, 1), (1, 300), (300, 1), (64, 64), (128, 128), (200, 333), (257, 12
           (1000, 77), (33, 1031)]
 
 
-VEC_SHAPES = {U32: [(128, 64), (64, 128), (128, 128)], U16: [(256, 128), (128, 256)]}
+VEC_SHAPES = {U32: [(128, 64), (64, 128), (128, 128), (128, 32)],
+              U16: [(256, 128), (128, 256), (256, 64)]}
 VEC_128 = {U32: [(64, 64), (32, 64), (128, 64)], U16: [(128, 128), (64, 128)]}
 VEC_SMALL = {U32: [(64, 32, 64), (64, 64, 32), (32, 32, 32)],
              U16: [(64, 64, 128), (64, 128, 64), (32, 64, 64)]}  # threads, rows, cols
