@@ -174,15 +174,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
             const char *why = nullptr;
             e = launch_tma(p, cfg, &why);
             if (e != cudaSuccess && why) {
-                const bool auto_mode = !o || o->variant == TR_VARIANT_AUTO;
-                if (auto_mode) {
-                    // The planner's first choice could not be encoded (e.g. a
-                    // plane pitch the tensor map rejects): take the LSU tile.
-                    VecConfig vc{cfg.tile_order, 0, 0, false, 0};
-                    auto_vec_shape(p, out16, &vc.tile_rows, &vc.tile_cols);
-                    e = launch_tile_vec(p, in16, out16, vc, &why);
-                    break;
-                }
+                // e.g. a plane pitch the tensor map cannot describe
                 set_error(why, cudaSuccess);
                 return TR_ERR_UNSUPPORTED;
             }
