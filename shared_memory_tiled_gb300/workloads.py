@@ -22,7 +22,9 @@ The workloads follow the five configurations the library is measured on:
 * ``c3``         fp32 12289x7919 with input row pitch 7936, N(0, 1) from seed 2;
 * ``c4``         batched fp32 [64, 2048, 1536] -> [64, 1536, 2048], uniform from seed 3;
 * ``c5``         bf16 16384x16384 (512 MiB), uniform random 16-bit patterns
-  from seed 4 (NaN and Inf patterns included).
+  from seed 4 (NaN and Inf patterns included);
+* ``c3_back``    c3's transpose back: 7919x12289 with input pitch 12289 (rows
+  start at every 4-byte offset from a 16-byte boundary) and output pitch 7936.
 """
 from __future__ import annotations
 
@@ -102,6 +104,8 @@ WORKLOADS = {
     "c3": Workload("c3", "f32", 12289, 7919, 7936, 12289, dist="normal", seed=2),
     "c4": Workload("c4", "f32", 2048, 1536, 1536, 2048, batch=64, dist="uniform", seed=3),
     "c5": Workload("c5", "bf16", 16384, 16384, 16384, 16384, dist="bits", seed=4),
+    # c3 transposed back: the odd pitch is now on the input side
+    "c3_back": Workload("c3_back", "f32", 7919, 12289, 12289, 7936, dist="normal", seed=2),
 }
 
 DESCRIPTION = {
@@ -111,6 +115,7 @@ DESCRIPTION = {
     "c3": "fp32 12289x7919 rectangular, N(0,1) seed 2, ld_in = 7936, output dense",
     "c4": "batched fp32 [64,2048,1536] -> [64,1536,2048], uniform[-1,1) seed 3, contiguous",
     "c5": "bf16 16384x16384 (512 MiB) square, uniform random u16 bits seed 4",
+    "c3_back": "fp32 7919x12289 (c3's output shape), input pitch 12289, output pitch 7936, N(0,1) seed 2",
 }
 
 
