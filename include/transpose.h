@@ -132,29 +132,46 @@ typedef struct tr_args {
     tr_stream_t stream;
 } tr_args;
 
-/* Single-matrix transpose of fp32 bit patterns (rows x cols -> cols x rows). */
+/* Single-matrix transpose of fp32 bit patterns: out[j*ld_out + i] = in[i*ld_in + j]
+ * for i < rows, j < cols ("Shared memory and the bank conflict", "Turn the tile
+ * around on chip": read a tile by rows, turn it around on chip, write it by
+ * rows).  `in` is rows x cols with row pitch ld_in (>= cols), `out` is cols x
+ * rows with row pitch ld_out (>= rows); both device memory owned by the caller.
+ * Errors: TR_ERR_BAD_DIM, TR_ERR_BAD_LD, TR_ERR_NULL, TR_ERR_OVERLAP before any
+ * launch, TR_ERR_CUDA if the launch fails (conventions at the top). */
 tr_status tr_transpose_f32(const float *in, float *out, int64_t rows, int64_t cols,
                            int64_t ld_in, int64_t ld_out, tr_stream_t stream);
 
-/* Single-matrix transpose of bf16 bit patterns (`in`/`out` point at 16-bit elements). */
+/* Single-matrix transpose of bf16 bit patterns (`in`/`out` point at 16-bit
+ * elements, moved as raw 16-bit words -- never converted, so every NaN payload
+ * survives); otherwise exactly tr_transpose_f32. */
 tr_status tr_transpose_bf16(const void *in, void *out, int64_t rows, int64_t cols,
                             int64_t ld_in, int64_t ld_out, tr_stream_t stream);
 
 /* Batched transpose [batch, rows, cols] -> [batch, cols, rows] of fp32 bit
- * patterns; plane b of the input starts at in + b*stride_in, of the output at
- * out + b*stride_out (elements). */
+ * patterns: each plane is transposed as in tr_transpose_f32; plane b of the
+ * input starts at in + b*stride_in, of the output at out + b*stride_out
+ * (elements).  For batch > 1 the plane pitches must keep planes apart
+ * (stride_in >= (rows-1)*ld_in + cols, stride_out >= (cols-1)*ld_out + rows,
+ * else TR_ERR_BAD_LD); no byte of the input extent may overlap the output
+ * extent (TR_ERR_OVERLAP). */
 tr_status tr_transpose_batched_f32(const float *in, float *out, int64_t batch, int64_t rows,
                                    int64_t cols, int64_t ld_in, int64_t ld_out,
                                    int64_t stride_in, int64_t stride_out, tr_stream_t stream);
 
-/* Batched transpose of bf16 bit patterns; same arguments as the fp32 form. */
+/* Batched transpose of bf16 bit patterns; same arguments, layout and errors
+ * as the fp32 form. */
 tr_status tr_transpose_batched_bf16(const void *in, void *out, int64_t batch, int64_t rows,
                                     int64_t cols, int64_t ld_in, int64_t ld_out,
                                     int64_t stride_in, int64_t stride_out, tr_stream_t stream);
 
-/* Any transpose with an explicit variant and tuning (opts may be NULL = AUTO).
- * Returns TR_ERR_UNSUPPORTED when the requested variant cannot run on these
- * arguments (e.g. TMA with a pitch that is not a multiple of 16 bytes). */
+/* Any transpose of the forms above with an explicit variant and tuning
+ * (`args` carries the element type, sizes, pitches and stream; `opts` may be
+ * NULL = AUTO).  Same result and argument errors as the fixed entry points;
+ * TR_ERR_UNSUPPORTED when an option is out of range or the requested variant
+ * cannot run on these arguments (e.g. TMA with a pitch that is not a multiple
+ * of 16 bytes, or a tile shape the variant does not have); tr_last_error()
+ * then says which. */
 tr_status tr_transpose_ex(const tr_args *args, const tr_options *opts);
 
 /* In-place transpose of `batch` square n x n planes of fp32 bit patterns:
