@@ -236,6 +236,15 @@ int32_t tr_plan_variant(const tr_args *args, const tr_options *opts);
  * the last call, TR_OK otherwise (TR_ERR_CUDA if the read itself fails). */
 tr_status tr_device_status(void);
 
+/* Exercises the failure path of the bounded in-kernel waits without any
+ * fault: one warp waits on an mbarrier phase that completes only when
+ * `arrive` is nonzero.  With arrive == 0 the wait runs out after limit_ns
+ * nanoseconds (1 ns .. 2 s, else TR_ERR_BAD_DIM), the kernel raises the same
+ * device fault flag the transpose kernels raise and returns, so a following
+ * tr_device_status() reports TR_ERR_TIMEOUT; with arrive != 0 it reports TR_OK.
+ * Asynchronous on `stream`. */
+tr_status tr_selftest_bounded_wait(int32_t arrive, int64_t limit_ns, tr_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *tr_status_string(tr_status status);
 

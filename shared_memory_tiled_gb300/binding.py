@@ -94,6 +94,7 @@ SIGNATURES = {
     "tr_operand_tiles_f32": ([VP, VP, I64, I64, I64, ctypes.c_int32, ctypes.c_int32,
                               ctypes.c_int32, VP], ctypes.c_int),
     "tr_device_status": ([], ctypes.c_int),
+    "tr_selftest_bounded_wait": ([ctypes.c_int32, I64, VP], ctypes.c_int),
     "tr_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tr_last_error": ([], ctypes.c_char_p),
     "tr_version": ([], ctypes.c_int32),
@@ -186,6 +187,10 @@ def tr_operand_tiles_f32(a_ptr, out_ptr, m, k, lda, bm, bk, pad=-1, stream=0) ->
 
 def tr_bank_probe(layout, reps, blocks, result_ptr, stream=0) -> int:
     return _call("tr_bank_probe", layout, reps, blocks, result_ptr, stream)
+
+
+def tr_selftest_bounded_wait(arrive, limit_ns, stream=0) -> int:
+    return _call("tr_selftest_bounded_wait", arrive, limit_ns, stream)
 
 
 def tr_device_status() -> int:

@@ -369,6 +369,17 @@ int32_t tr_plan_variant(const tr_args *args, const tr_options *opts) {
     return tr::choose(p, opts);
 }
 
+tr_status tr_selftest_bounded_wait(int32_t arrive, int64_t limit_ns, tr_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > 2000000000LL) return TR_ERR_BAD_DIM;
+    const cudaError_t e =
+        tr::launch_wait_selftest(arrive != 0, limit_ns, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tr::set_error("self-test launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
 tr_status tr_device_status(void) {
     unsigned v = 0;
     const cudaError_t e = tr::read_and_clear_fault(&v);

@@ -752,6 +752,33 @@ cudaError_t launch_tma(const Problem &p, const TmaConfig &cfg, const char **why)
     return p.esize == 4 ? launch_typed<uint32_t>(p, cfg, why) : launch_typed<uint16_t>(p, cfg, why);
 }
 
+namespace {
+
+// Self-test of the bounded wait: one warp waits on an mbarrier phase that
+// completes only if `arrive` is set (lane 0 arrives on it); otherwise the
+// wait runs out after limit_ns and the fault flag is raised exactly as in the
+// transpose kernels.  Nothing here can fault or hang: the wait is bounded.
+__global__ void k_wait_selftest(int arrive, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    if (arrive && threadIdx.x == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_addr(&bar))
+                     : "memory");
+    const bool ok = ptx::mbar_wait_bounded(&bar, 0, limit_ns);
+    if (__any_sync(0xffffffffu, !ok) && threadIdx.x == 0) atomicExch(&g_fault_flag, 1u);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(bool arrive, int64_t limit_ns, cudaStream_t stream) {
+    k_wait_selftest<<<1, 32, 0, stream>>>(arrive ? 1 : 0, uint64_t(limit_ns));
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_fault(unsigned *value) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;

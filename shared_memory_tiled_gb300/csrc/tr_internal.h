@@ -63,6 +63,10 @@ cudaError_t launch_operand_tiles(const uint32_t *a, uint32_t *out, int64_t m, in
 cudaError_t launch_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
                            int64_t stride, cudaStream_t stream);
 
+// One warp waiting on an mbarrier that completes only when `arrive` is set;
+// otherwise the bounded wait runs out after limit_ns and raises the fault flag.
+cudaError_t launch_wait_selftest(bool arrive, int64_t limit_ns, cudaStream_t stream);
+
 // Device-side fault flag (bounded waits that ran out).  Reads and clears it.
 cudaError_t read_and_clear_fault(unsigned *value);
 

@@ -180,3 +180,8 @@ def test_bank_probe_argument_errors(lib):
     assert B.tr_bank_probe(0, -1, 1, FAKE_OUT) == B.Status.ERR_BAD_DIM
     assert B.tr_bank_probe(0, 1, 1, 0) == B.Status.ERR_NULL
     assert B.tr_bank_probe(0, 1, 0, 0) == B.Status.OK
+
+
+def test_selftest_argument_errors_on_host(lib):
+    assert B.tr_selftest_bounded_wait(0, 0) == B.Status.ERR_BAD_DIM
+    assert B.tr_selftest_bounded_wait(1, -5) == B.Status.ERR_BAD_DIM
