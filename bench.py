@@ -214,7 +214,6 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = W.WORKLOADS[args.workload]
-    import numpy as np  # noqa: F401
     x = W.make_input(w)
     for _ in range(args.warmup):
         time_oracle(w, 0.0, max_reps=1, x=x)

@@ -2,7 +2,6 @@
 rejects bad arguments before any CUDA call (no GPU needed)."""
 from __future__ import annotations
 
-import ctypes
 import os
 import re
 

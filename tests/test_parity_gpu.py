@@ -3,7 +3,6 @@ the C ABI.  The whole output buffer is compared, pitch padding included (it
 must keep its prefill)."""
 from __future__ import annotations
 
-import itertools
 
 import numpy as np
 import pytest
