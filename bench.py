@@ -448,6 +448,8 @@ def run_ours(args):
         "pct_of_hbm_nominal": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_copy": round(100 * gbs / (copy_gbs * world), 2),
         "median_step_ms": round(med_ms, 5),
+        "min_step_ms": round(min(per_ms), 5),
+        "p90_step_ms": round(sorted(per_ms)[int(0.9 * (len(per_ms) - 1))], 5),
         "copy": {"value": round(copy_gbs, 2), "unit": "GB/s", "bytes_per_step": 2 * copy_bytes,
                  "kernel": "tr_copy", "torch_copy_GBps": round(torch_copy_gbs, 2)},
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 2), "peak": peak,
