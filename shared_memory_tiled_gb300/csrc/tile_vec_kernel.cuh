@@ -38,9 +38,10 @@
 // elements before the row's first 16-byte boundary inside the tile, and lane A
 // stores the aligned chunk made of its own last V-d elements and the first d
 // of lane A+1 (fetched with a warp shuffle); the d head elements and the V-d
-// tail elements of the tile's row segment go out as single elements.  Partial
-// tiles at the matrix edge always use bounds-checked element accesses except
-// where a whole chunk is in range on an aligned side.
+// tail elements of the tile's row segment go out as single elements.  Tiles at
+// the matrix edge use bounds-checked element accesses except where a whole
+// chunk is in range on an aligned side, or (shifted stores) where the tile's
+// output row segments are complete and only its last output rows are missing.
 #pragma once
 
 #include "tile_geom.cuh"
@@ -168,13 +169,18 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
 #pragma unroll
                 for (int m = 0; m < V; ++m)
                     __stcs(reinterpret_cast<uint4 *>(dst + (c0 + V * C + m) * g.ld_out + oc), y[m].v);
-            } else if (full) {
+            } else if (SHIFT_OUT && r0 + TR <= g.rows) {
+                // Every output row segment of the tile is complete (the tile may
+                // still stop short of the last output rows): shifted stores for
+                // the rows that exist.  The shuffles run on every lane.
 #pragma unroll
                 for (int m = 0; m < V; ++m) {
-                    T *row = dst + (c0 + V * C + m) * g.ld_out;
+                    const int64_t orow = c0 + V * C + m;
+                    T *row = dst + orow * g.ld_out;
                     Chunk nb;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) nb.w[k] = __shfl_down_sync(0xffffffffu, y[m].w[k], 1);
+                    if (!full && orow >= g.cols) continue;
                     const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
                     const int d = (V - s) % V;  // elements before the first 16-byte boundary
                     if (d == 0) {

@@ -124,7 +124,9 @@ def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
     """Odd output pitches: every output row starts at a different offset from a
     16-byte boundary (the shifted-store path), full tiles and ragged edges."""
     for (b, r, c, pi, po, pp) in [(1, 515, 300, 4, 1, 0), (2, 256, 256, 0, 3, 5),
-                                  (1, 1025, 263, 9, 0, 0), (3, 130, 129, 7, 2, 1)]:
+                                  (1, 1025, 263, 9, 0, 0), (3, 130, 129, 7, 2, 1),
+                                  (1, 515, 300, 4, 2, 0), (2, 256, 200, 0, 1, 3),
+                                  (1, 384, 70, 0, 5, 0)]:
         x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=r + c)
         for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC),
                    dict(variant=V.TILE_VEC, schedule=2)] + \
