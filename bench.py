@@ -63,6 +63,7 @@ KERNEL_SOURCES = {
     "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
     "k_tma_warp": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
     "k_tma_ldst": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
+    "k_tma_ws": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
     "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
     "k_copy_aligned": ["copy.cu", "tr_internal.h"],
@@ -492,7 +493,7 @@ def run_ours(args):
         raise SystemExit("bench: end-to-end output differs from the transposed input")
 
     peak, peak_kind = read_peaks()
-    kname = {B.Variant.TMA: {1: "k_tma", 3: "k_tma_ldst"}.get(args.schedule, "k_tma_warp"),
+    kname = {B.Variant.TMA: {1: "k_tma", 3: "k_tma_ldst", 4: "k_tma_ws"}.get(args.schedule, "k_tma_warp"),
              B.Variant.TILE_VEC: "k_tile_vec", B.Variant.TILE_PAD: "k_tile_pad",
              B.Variant.NAIVE_ROW: "k_naive", B.Variant.NAIVE_COL: "k_naive"}.get(planned, "?")
     if inplace:

@@ -115,7 +115,11 @@ typedef struct tr_options {
                            *   128x128 bf16 tiles, one block barrier per tile),
                            *   2 = one pipeline per warp (32x32 fp32 / 64x64 bf16 tiles),
                            *   3 = per-warp TMA loads, register transpose and 16-byte
-                           *       global stores (no output buffer, no TMA store)        */
+                           *       global stores (no output buffer, no TMA store),
+                           *   4 = warp-specialised: one producer warp keeps up to
+                           *       `stages` 64x64 fp32 / 128x128 bf16 tile loads in
+                           *       flight on full/empty mbarriers, eight consumer warps
+                           *       transpose and store with 16-byte global stores     */
     int32_t threads;      /* TILE_VEC: threads per block, 32, 64, 128 or 256, 0 = default */
 } tr_options;
 

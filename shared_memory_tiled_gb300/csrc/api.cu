@@ -97,7 +97,7 @@ bool options_valid(const tr_options *o) {
     if (o->out_stages != 0 && (o->out_stages < 2 || o->out_stages > 4)) return false;
     if (o->tile_rows < 0 || o->tile_cols < 0 || o->tile_rows > 256 || o->tile_cols > 256)
         return false;
-    if (o->schedule < 0 || o->schedule > 3) return false;
+    if (o->schedule < 0 || o->schedule > 4) return false;
     if (o->threads != 0 && o->threads != 32 && o->threads != 64 && o->threads != 128 &&
         o->threads != 256)
         return false;
@@ -151,8 +151,8 @@ tr_status run(const tr_args *a, const tr_options *o) {
         case TR_VARIANT_NAIVE_COL: e = launch_naive(p, false); break;
         case TR_VARIANT_TILE_PAD: e = launch_tile_pad(p, o ? o->pad : 1); break;
         case TR_VARIANT_TILE_VEC: {
-            if (o && o->schedule == 3) {
-                set_error("schedule 3 (TMA loads, register stores) belongs to the TMA variant",
+            if (o && o->schedule >= 3) {
+                set_error("schedules 3 and 4 (TMA load pipelines) belong to the TMA variant",
                           cudaSuccess);
                 return TR_ERR_UNSUPPORTED;
             }

@@ -528,6 +528,147 @@ k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised pipeline: one producer warp and eight consumer warps per
+// CTA, over the CTA-wide 16V x 16V tiles (two 128-byte boxes per tile).
+//
+// Each input slot has two mbarriers.  `full[slot]` completes when the TMA
+// bytes of the tile have landed (the producer arms it with expect_tx);
+// `empty[slot]` completes when all eight consumer warps have read the slot
+// (one arrival per warp).  The producer (lane 0 of the last warp) walks the
+// CTA's tiles, waits for a slot to be empty and refills it, so up to S tile
+// loads are in flight while the consumers work; it never touches the data.
+// The consumers wait for a slot to be full, read their micro-block, release
+// the slot and store the transposed micro-block straight to global memory
+// with 16-byte stores.  No consumer waits for another: the only coupling is
+// through the slot barriers ("Shared-memory tiling and bank conflicts",
+// "Protect tile phases": a buffer is refilled only after its readers are
+// done, and read only after its writer is done).
+//
+// Consumer thread t (< 256) owns micro-block (A, C) = (t % 16, t / 16): tile
+// rows V*A .. V*A+V-1 of chunk column C, which become output rows V*C + m,
+// chunk A; sixteen lanes with consecutive A write 256 contiguous bytes of one
+// output row.  The 8 lanes of a shared-load phase share C and have A = 8h ..
+// 8h+7; reading row V*A + m for the same m in every lane would put them on 2
+// (fp32) or 1 (bf16) swizzle positions, so lane A reads its rows rotated by
+// rot = (A / 2) % 4 (fp32) or A % 8 (bf16), which makes row % 8 -- and with
+// it the position chunk ^ (row % 8) -- distinct across the phase; the rotation
+// is undone in registers.
+constexpr int kWsConsumerWarps = 8;
+constexpr int kWsThreads = 32 * (kWsConsumerWarps + 1);
+
+template <typename T>
+__global__ void __launch_bounds__(kWsThreads, 1)
+k_tma_ws(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
+    using L = TmaTile<T>;
+    constexpr int V = L::V;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = g.in_stages;
+    uint8_t *in_buf = base;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + size_t(S) * L::BUF_BYTES);
+    uint64_t *empty = full + S;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t n_local =
+        blockIdx.x < g.total ? (g.total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (t == 0) {
+        ptx::prefetch_tensormap(&tm_in);
+        for (int i = 0; i < S; ++i) {
+            ptx::mbar_init(full + i, 1);
+            ptx::mbar_init(empty + i, kWsConsumerWarps);
+        }
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kWsConsumerWarps) {
+        // ---- producer
+        if (lane != 0) return;
+        int64_t k = 0;
+        bool ok = true;
+        for (; k < n_local; ++k) {
+            const int slot = int(k % S);
+            // Slot reuse: the consumers must have released the tile loaded
+            // into it S tiles ago (phase k/S - 1 of its empty barrier).
+            if (k >= S && !ptx::mbar_wait_bounded(empty + slot, uint32_t((k / S - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            int32_t b, tr, tc;
+            tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
+            uint8_t *dst = in_buf + size_t(slot) * L::BUF_BYTES;
+            ptx::mbar_arrive_expect_tx(full + slot, L::BUF_BYTES);
+            ptx::tma_load_3d(dst, &tm_in, full + slot, tc * L::TILE, tr * L::TILE, b);
+            ptx::tma_load_3d(dst + L::BOX_BYTES, &tm_in, full + slot, tc * L::TILE + L::BOXC,
+                             tr * L::TILE, b);
+        }
+        if (!ok) atomicExch(&g_fault_flag, 1u);
+        // The last load issued into each slot lands before the CTA's shared
+        // memory can go away (no later phase starts, so the parity is exact).
+        for (int64_t kk = k > S ? k - S : 0; kk < k; ++kk)
+            ptx::mbar_wait_bounded(full + int(kk % S), uint32_t((kk / S) & 1));
+        return;
+    }
+
+    // ---- consumers
+    const int A = t & 15, C = t >> 4;
+    const int rot = V == 4 ? ((A >> 1) & 3) : (A & 7);
+    uint32_t roff[V];
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const int r = V * A + ((m + rot) & (V - 1));
+        roff[m] = (C >> 3) * L::BOX_BYTES + r * 128 + (((C & 7) ^ (r & 7)) << 4);
+    }
+    for (int64_t k = 0; k < n_local; ++k) {
+        const int slot = int(k % S);
+        const bool ok = ptx::mbar_wait_bounded(full + slot, uint32_t((k / S) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            // The producer's own bounded wait for this warp's release runs out
+            // in turn and drains the loads in flight.
+            if (lane == 0) atomicExch(&g_fault_flag, 1u);
+            break;
+        }
+        const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
+        uint4 x[V];
+#pragma unroll
+        for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty + slot);
+
+        int32_t b, tr, tc;
+        tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
+        unrotate<V>(x, rot);
+        uint4 y[V];
+        micro_transpose(x, y);
+        T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
+        const int64_t r0 = int64_t(tr) * L::TILE, c0 = int64_t(tc) * L::TILE;
+        const bool full_tile = r0 + L::TILE <= g.rows && c0 + L::TILE <= g.cols;
+        const int64_t oc = r0 + V * A;
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+            const int64_t orow = c0 + V * C + m;
+            T *row = dst + orow * g.ld_out;
+            if (full_tile) {
+                __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+            } else if (orow < g.cols) {
+                if (oc + V <= g.rows) {
+                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                } else {
+                    const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
+#pragma unroll
+                    for (int e = 0; e < V; ++e)
+                        if (oc + e < g.rows) {
+                            const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
+                            row[oc + e] = T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
+                        }
+                }
+            }
+        }
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -567,7 +708,7 @@ bool encode_3d(CUtensorMap *map, const void *base, int esize, int64_t elems, int
 
 // Per-device facts and per-configuration occupancy, computed once: the
 // launch path then makes no attribute or occupancy query per call.
-enum Kind { kPerBlock = 0, kPerWarp = 1, kLoadOnly = 2 };
+enum Kind { kPerBlock = 0, kPerWarp = 1, kLoadOnly = 2, kWarpSpec = 3 };
 
 struct DeviceInfo {
     std::atomic<bool> ok{false};  // set last, after the fields below are filled
@@ -575,7 +716,7 @@ struct DeviceInfo {
     int sms = 0;
     int max_smem_optin = 0;
     // [kind][esize == 4][in_stages][out_stages]; 0 = not computed
-    std::atomic<int> fit[3][2][9][kMaxOutStages + 1] = {};
+    std::atomic<int> fit[4][2][9][kMaxOutStages + 1] = {};
 };
 
 constexpr int kMaxDevices = 64;
@@ -601,12 +742,14 @@ DeviceInfo &device_info() {
             if (e == cudaSuccess)
                 e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
             // Opt the kernels in to the largest dynamic shared memory once.
-            const void *kernels[6] = {reinterpret_cast<const void *>(k_tma<uint32_t>),
+            const void *kernels[8] = {reinterpret_cast<const void *>(k_tma<uint32_t>),
                                       reinterpret_cast<const void *>(k_tma<uint16_t>),
                                       reinterpret_cast<const void *>(k_tma_warp<uint32_t>),
                                       reinterpret_cast<const void *>(k_tma_warp<uint16_t>),
                                       reinterpret_cast<const void *>(k_tma_ldst<uint32_t>),
-                                      reinterpret_cast<const void *>(k_tma_ldst<uint16_t>)};
+                                      reinterpret_cast<const void *>(k_tma_ldst<uint16_t>),
+                                      reinterpret_cast<const void *>(k_tma_ws<uint32_t>),
+                                      reinterpret_cast<const void *>(k_tma_ws<uint16_t>)};
             for (const void *k : kernels)
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -634,6 +777,8 @@ size_t smem_bytes(Kind kind, int in_stages, int out_stages) {
         case kPerWarp:
             return 1024 + size_t(kWarpsPerBlock) * (size_t(in_stages + out_stages) *
                                                         WarpTile<T>::BYTES + size_t(in_stages) * 8);
+        case kWarpSpec:  // input slots, a full and an empty barrier per slot
+            return 1024 + size_t(in_stages) * TmaTile<T>::BUF_BYTES + size_t(in_stages) * 16;
         default:
             return 1024 + size_t(kWarpsPerBlock) *
                               (size_t(in_stages) * WarpTile<T>::BYTES + size_t(in_stages) * 8);
@@ -653,6 +798,8 @@ int resident_ctas(DeviceInfo &dev, Kind kind, int in_stages, int out_stages) {
         else if (kind == kPerWarp)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_warp<T>,
                                                               32 * kWarpsPerBlock, smem);
+        else if (kind == kWarpSpec)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_ws<T>, kWsThreads, smem);
         else
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k_tma_ldst<T>,
                                                               32 * kWarpsPerBlock, smem);
@@ -665,10 +812,12 @@ int resident_ctas(DeviceInfo &dev, Kind kind, int in_stages, int out_stages) {
 // Defaults, the best measured on GB300: per-warp pipeline with 6 box loads
 // in flight and 2 output buffers (fp32, 4 KiB boxes) or 4 loads and 3 output
 // buffers (bf16, 8 KiB boxes); CTA-wide pipeline with 2 + 2; load-only
-// pipeline with 8 (fp32) or 6 (bf16) loads in flight.
+// pipeline with 8 (fp32) or 6 (bf16) loads in flight; warp-specialised
+// pipeline with 8 tile slots (fp32, one CTA per SM) or 2 (bf16).
 int default_in_stages(size_t esize, Kind kind) {
     if (kind == kPerWarp) return esize == 4 ? 6 : 4;
     if (kind == kLoadOnly) return esize == 4 ? 8 : 6;
+    if (kind == kWarpSpec) return esize == 4 ? 8 : 2;
     return 2;
 }
 int default_out_stages(size_t esize, Kind kind) {
@@ -677,8 +826,12 @@ int default_out_stages(size_t esize, Kind kind) {
 
 template <typename T>
 cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **why) {
-    const Kind kind = cfg.schedule == 1 ? kPerBlock : cfg.schedule == 3 ? kLoadOnly : kPerWarp;
-    const int tile = kind == kPerBlock ? TmaTile<T>::TILE : WarpTile<T>::TILE;
+    const Kind kind = cfg.schedule == 1   ? kPerBlock
+                      : cfg.schedule == 3 ? kLoadOnly
+                      : cfg.schedule == 4 ? kWarpSpec
+                                          : kPerWarp;
+    const bool cta_tile = kind == kPerBlock || kind == kWarpSpec;
+    const int tile = cta_tile ? TmaTile<T>::TILE : WarpTile<T>::TILE;
     const int boxc = TmaTile<T>::BOXC;  // 128-byte box rows in every kind
     const int64_t two31 = int64_t(1) << 31, two40 = int64_t(1) << 40;
     if (p.rows >= two31 || p.cols >= two31 || p.batch >= two31) {
@@ -696,7 +849,7 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     }
     CUtensorMap tm_in, tm_out;
     if (!encode_3d(&tm_in, p.in, p.esize, p.cols, p.rows, p.batch, p.ld_in, sin, boxc, tile) ||
-        (kind != kLoadOnly &&
+        (kind != kLoadOnly && kind != kWarpSpec &&
          !encode_3d(&tm_out, p.out, p.esize, p.rows, p.cols, p.batch, p.ld_out, sout, boxc, tile))) {
         *why = "cuTensorMapEncodeTiled rejected the tensor maps";
         return cudaErrorInvalidValue;
@@ -734,13 +887,15 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     }
     int per_sm = cfg.ctas_per_sm > 0 ? cfg.ctas_per_sm : fit;
     if (per_sm > fit) per_sm = fit;
-    const int64_t units = kind == kPerBlock ? g.total : (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t units = cta_tile ? g.total : (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock;
     int64_t grid = int64_t(dev.sms) * per_sm;
     if (grid > units) grid = units;
     if (kind == kPerWarp)
         k_tma_warp<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, tm_out, g);
     else if (kind == kLoadOnly)
         k_tma_ldst<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, g);
+    else if (kind == kWarpSpec)
+        k_tma_ws<T><<<unsigned(grid), kWsThreads, smem, p.stream>>>(tm_in, g);
     else
         k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
     return cudaGetLastError();

@@ -25,7 +25,8 @@ struct TmaConfig {
     int tile_order;    // 0 row-major, 1 diagonal
     int out_stages;    // output buffers, 0 = default
     int schedule;      // 0 default (per-warp), 1 CTA-wide pipeline, 2 per-warp pipelines,
-                       // 3 per-warp TMA loads with register stores
+                       // 3 per-warp TMA loads with register stores, 4 warp-specialised
+                       // producer warp + consumer warps with register stores
 };
 
 // True when the side's base pointer, row pitch and (for batch > 1) plane pitch

@@ -126,6 +126,7 @@ def test_planner(lib):
     assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, variant=9) == -B.Status.ERR_UNSUPPORTED
     assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, stages=1) == -B.Status.ERR_UNSUPPORTED
     assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, pad=5) == -B.Status.ERR_UNSUPPORTED
+    assert _plan(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, schedule=5) == -B.Status.ERR_UNSUPPORTED
     assert _plan(FAKE_IN, FAKE_OUT, 7, 1, 4, 4, 4, 4) == -B.Status.ERR_UNSUPPORTED
 
 
@@ -134,6 +135,11 @@ def test_ex_rejects_bad_options_and_reserved_fields(lib):
     assert B.tr_transpose_ex(a, B.make_options(variant=42)) == B.Status.ERR_UNSUPPORTED
     o = B.make_options(threads=64)
     assert B.tr_transpose_ex(a, o) == B.Status.ERR_UNSUPPORTED
+    # the TMA load pipelines (schedules 3 and 4) are refused for the LSU tile,
+    # on the host, before any CUDA call
+    for sched in (3, 4):
+        o = B.make_options(B.Variant.TILE_VEC, schedule=sched)
+        assert B.tr_transpose_ex(a, o) == B.Status.ERR_UNSUPPORTED
     a.reserved = 1
     assert B.tr_transpose_ex(a, None) == B.Status.ERR_UNSUPPORTED
     assert B.tr_transpose_ex(B.make_args(0, 0, B.DType.F32, 0, 0, 0, 0, 0)) == B.Status.OK

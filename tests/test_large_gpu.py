@@ -27,7 +27,7 @@ def _sampled_check(x, out, rows, cols, ld_in, ld_out, n=1 << 16, seed=0):
 
 
 @pytest.mark.parametrize("variant,schedule", [(B.Variant.AUTO, 0), (B.Variant.TMA, 0),
-                                              (B.Variant.TMA, 3)])
+                                              (B.Variant.TMA, 3), (B.Variant.TMA, 4)])
 def test_fp32_beyond_2_31_elements(variant, schedule):
     import torch
     rows, cols = 65537, 32801          # 2,149,679,137 elements, 8.6 GB each way

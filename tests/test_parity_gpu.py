@@ -72,7 +72,10 @@ def _variants(dtype, aligned):
                                                      out_stages=3),
                dict(variant=V.TMA, schedule=1, stages=deep, tile_order=1),
                dict(variant=V.TMA, schedule=3), dict(variant=V.TMA, schedule=3, stages=2),
-               dict(variant=V.TMA, schedule=3, stages=8, tile_order=1)]
+               dict(variant=V.TMA, schedule=3, stages=8, tile_order=1),
+               dict(variant=V.TMA, schedule=4), dict(variant=V.TMA, schedule=4, stages=2),
+               dict(variant=V.TMA, schedule=4, stages=3, ctas_per_sm=1),
+               dict(variant=V.TMA, schedule=4, stages=deep + 2, tile_order=1)]
     return vs
 
 
@@ -148,6 +151,9 @@ def test_tma_stage_count_that_does_not_fit_is_refused():
     with pytest.raises(B.TransposeError) as e:
         gpu_out(x, prefill, *geo, variant=V.TMA, schedule=1, stages=8)  # 10 x 32 KiB
     assert e.value.status == B.Status.ERR_UNSUPPORTED
+    with pytest.raises(B.TransposeError) as e:
+        gpu_out(x, prefill, *geo, variant=V.TMA, schedule=4, stages=8)  # 8 x 32 KiB
+    assert e.value.status == B.Status.ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("dtype", [U32, U16], ids=["f32", "bf16"])
@@ -172,8 +178,9 @@ def test_nan_payloads_survive_every_variant():
 
 
 @pytest.mark.parametrize("variant", [dict(variant=V.TILE_PAD, pad=1), dict(variant=V.TILE_VEC),
-                                     dict(variant=V.TMA), dict(variant=V.TMA, schedule=3)],
-                         ids=["pad1", "vec", "tma", "tma_ldst"])
+                                     dict(variant=V.TMA), dict(variant=V.TMA, schedule=3),
+                                     dict(variant=V.TMA, schedule=4)],
+                         ids=["pad1", "vec", "tma", "tma_ldst", "tma_ws"])
 def test_index_check_repeated(variant):
     """The exact index check run many times: a tile read before it was fully
     written fails it ("Shared memory and the bank conflict", "The barrier")."""
@@ -212,7 +219,8 @@ def test_workload_full_size(name):
     kws += [dict(variant=V.TILE_VEC, threads=n, tile_rows=r, tile_cols=c)
             for n, r, c in VEC_SMALL[U32 if es == 4 else U16]]
     if aligned:
-        kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1), dict(variant=V.TMA, schedule=3)]
+        kws += [dict(variant=V.TMA), dict(variant=V.TMA, schedule=1), dict(variant=V.TMA, schedule=3),
+                dict(variant=V.TMA, schedule=4)]
     if name.startswith("c1"):
         kws += [dict(variant=V.TILE_PAD, pad=0), dict(variant=V.TILE_PAD, pad=1),
                 dict(variant=V.TILE_PAD, pad=2), dict(variant=V.NAIVE_ROW),
