@@ -117,16 +117,17 @@ int32_t choose(const Problem &p, const tr_options *o) {
 }
 
 // Tile shape AUTO uses for the vectorised tile (measured on GB300).  Output
-// rows that are not 16-byte aligned pay a few single-element stores at both
-// ends of every row segment, so they take tiles twice as tall (longer output
-// segments: 12289x7919 fp32 91.6% of the copy with 128x64 against 75% with
-// 64x64).  A misaligned input is read one element at a time, which wants
-// tiles twice as wide (7919x12289 with pitch 12289: 95.7% with 64x128
-// against 88.6% with 64x64).
+// rows that are not 16-byte aligned (shifted stores) take 128-row tiles, 16
+// chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s with
+// 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16 with
+// output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128.  A
+// misaligned input is read one element at a time, which wants tiles twice as
+// wide (7919x12289 with pitch 12289: 95.7% of the copy with 64x128 against
+// 88.6% with 64x64).
 void auto_vec_shape(const Problem &p, bool in16, bool out16, int *rows, int *cols) {
     const int v = 16 / p.esize;  // elements per 16-byte chunk
     if (!out16) {
-        *rows = 32 * v;
+        *rows = 128;
         *cols = 16 * v;
     } else if (!in16) {
         *rows = 16 * v;

@@ -34,14 +34,19 @@
 //
 // Misaligned sides.  VEC_IN = false loads single elements (any pitch).  With
 // SHIFT_OUT the output rows need not start on 16-byte boundaries (e.g. a row
-// pitch of 12289 fp32): for each output row the block finds the number d of
-// elements before the row's first 16-byte boundary inside the tile, and lane A
-// stores the aligned chunk made of its own last V-d elements and the first d
-// of lane A+1 (fetched with a warp shuffle); the d head elements and the V-d
-// tail elements of the tile's row segment go out as single elements.  Tiles at
-// the matrix edge use bounds-checked element accesses except where a whole
-// chunk is in range on an aligned side, or (shifted stores) where the tile's
-// output row segments are complete and only its last output rows are missing.
+// pitch of 12289 fp32).  For each output row, d is the number of elements
+// between the tile's first column r0 and the row's next 16-byte boundary (the
+// same for every tile of the row), and the tile owns the output columns
+// [r0 + d, r0 + TR + d) -- plus [0, d) in the first tile row -- so every
+// store inside the matrix is a whole aligned chunk: lane A stores its own last
+// V-d elements followed by the first d of micro-block A+1, fetched from lane
+// A+1 with a warp shuffle or, for the last micro-block row, from V extra input
+// rows staged below the tile (the halo).  Single elements remain only at the
+// matrix edges (the first d columns, the columns past the last input row).
+// Tiles at the matrix edge use bounds-checked element accesses except where a
+// whole chunk is in range on an aligned side, or (shifted stores) where the
+// tile's output row segments are complete and only its last output rows are
+// missing.
 #pragma once
 
 #include "tile_geom.cuh"
@@ -86,7 +91,13 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     constexpr int LOADS = TR / RPP;          // chunks each thread loads
     static_assert(MR >= 8 && MR <= 32 && MC >= 8 && NT % MC == 0 && (MR * MC) % NT == 0,
                   "unsupported tile shape");
-    extern __shared__ uint4 smem[];          // TR rows of MC chunks
+    // With shifted stores the tile also stages the V input rows below it (the
+    // halo): the last lane of each micro-block row builds its output chunks
+    // from them (phase 2).
+    constexpr int HALO = SHIFT_OUT ? V : 0;       // extra tile rows
+    constexpr int HCH = HALO * MC;                // halo chunks
+    constexpr int HL = SHIFT_OUT ? (HCH + NT - 1) / NT : 1;  // halo chunks per thread
+    extern __shared__ uint4 smem[];          // TR + HALO rows of MC chunks
 
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
@@ -94,6 +105,7 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     // Phase 1a: this thread's chunks of tile `tile`, global -> registers, all
     // loads issued before any is used.
     Chunk ld[LOADS];
+    Chunk hl[HL];
     auto load_tile = [&](int64_t tile) {
         int64_t b, tr, tc;
         split_tile(g, tile, diagonal, b, tr, tc);
@@ -126,6 +138,32 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                 }
             }
         }
+        if constexpr (SHIFT_OUT) {
+            // Halo: input rows r0+TR .. r0+TR+V-1, bounds-checked (they lie
+            // past the matrix at its last tile rows; zeros are never stored).
+#pragma unroll
+            for (int k = 0; k < HL; ++k) {
+                const int h = t + NT * k;
+                if (HCH % NT != 0 && h >= HCH) continue;
+                const int64_t gr = r0 + TR + h / MC;
+                const int64_t hc = c0 + (h % MC) * V;
+                if (VEC_IN && gr < g.rows && hc + V <= g.cols) {
+                    hl[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + hc));
+                } else {
+                    T e[V];
+#pragma unroll
+                    for (int q = 0; q < V; ++q)
+                        e[q] = (gr < g.rows && hc + q < g.cols) ? src[gr * g.ld_in + hc + q] : T(0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (sizeof(T) == 4)
+                            hl[k].w[q] = uint32_t(e[q]);
+                        else
+                            hl[k].w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                    }
+                }
+            }
+        }
     };
 
     // With PREFETCH the grid is persistent and the loads of a block's next
@@ -152,6 +190,15 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
             const int r = lr + RPP * k;
             smem[r * MC + (lcc ^ ((r / V) & 7))] = ld[k].v;
         }
+        if constexpr (SHIFT_OUT) {
+#pragma unroll
+            for (int k = 0; k < HL; ++k) {
+                const int h = t + NT * k;
+                if (HCH % NT != 0 && h >= HCH) continue;
+                const int r = TR + h / MC;
+                smem[r * MC + ((h % MC) ^ ((r / V) & 7))] = hl[k].v;
+            }
+        }
         __syncthreads();
         if (PREFETCH && tile + gridDim.x < g.total) load_tile(tile + gridDim.x);
 
@@ -171,8 +218,14 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     __stcs(reinterpret_cast<uint4 *>(dst + (c0 + V * C + m) * g.ld_out + oc), y[m].v);
             } else if (SHIFT_OUT && r0 + TR <= g.rows) {
                 // Every output row segment of the tile is complete (the tile may
-                // still stop short of the last output rows): shifted stores for
-                // the rows that exist.  The shuffles run on every lane.
+                // still stop short of the last output rows).  For an output row
+                // whose first 16-byte boundary lies d elements past column r0,
+                // the tile owns columns [r0 + d, r0 + TR + d) (and [0, d) in
+                // the first tile row): lane A stores the aligned chunk made of
+                // its own last V-d elements and the first d of micro-block A+1,
+                // taken from lane A+1 by a warp shuffle or, for A = MR-1, from
+                // the halo micro-block below the tile.  The shuffles run on
+                // every lane.
 #pragma unroll
                 for (int m = 0; m < V; ++m) {
                     const int64_t orow = c0 + V * C + m;
@@ -180,23 +233,43 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     Chunk nb;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) nb.w[k] = __shfl_down_sync(0xffffffffu, y[m].w[k], 1);
+                    if (A == MR - 1) {
+                        // Column V*C+m of the halo rows TR .. TR+V-1, read as
+                        // single elements (one lane per micro-block row).
+                        const T *sm = reinterpret_cast<const T *>(smem);
+                        T e[V];
+#pragma unroll
+                        for (int q = 0; q < V; ++q) e[q] = sm[((TR + q) * MC + (C ^ (MR & 7))) * V + m];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if constexpr (sizeof(T) == 4)
+                                nb.w[q] = uint32_t(e[q]);
+                            else
+                                nb.w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                        }
+                    }
                     if (!full && orow >= g.cols) continue;
                     const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
                     const int d = (V - s) % V;  // elements before the first 16-byte boundary
                     if (d == 0) {
                         __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                        continue;
+                    }
+                    const int64_t wc = oc + d;  // first column of the aligned chunk
+                    Chunk wv;
+                    wv.v = window<T>(y[m], nb, d);
+                    if (wc + V <= g.rows) {
+                        __stcs(reinterpret_cast<uint4 *>(row + wc), wv.v);
                     } else {
-                        if (A < MR - 1)
-                            __stcs(reinterpret_cast<uint4 *>(row + oc + d), window<T>(y[m], nb, d));
-                        if (A == 0) {
+                        // the halo ran past the last input row
 #pragma unroll
-                            for (int q = 0; q < V; ++q)
-                                if (q < d) row[oc + q] = elem<T>(y[m], q);
-                        } else if (A == MR - 1) {
+                        for (int q = 0; q < V; ++q)
+                            if (wc + q < g.rows) row[wc + q] = elem<T>(wv, q);
+                    }
+                    if (tr == 0 && A == 0) {
 #pragma unroll
-                            for (int q = 0; q < V; ++q)
-                                if (q >= d) row[oc + q] = elem<T>(y[m], q);
-                        }
+                        for (int q = 0; q < V; ++q)
+                            if (q < d) row[q] = elem<T>(y[m], q);
                     }
                 }
             } else {
@@ -208,9 +281,18 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     if (!SHIFT_OUT && oc + V <= g.rows) {
                         __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
                     } else {
+                        // With shifted stores the first d columns of the segment
+                        // belong to the tile above (it wrote them from its halo).
+                        int64_t lo = 0;
+                        if constexpr (SHIFT_OUT) {
+                            if (tr > 0) {
+                                const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
+                                lo = r0 + (V - s) % V;
+                            }
+                        }
 #pragma unroll
                         for (int q = 0; q < V; ++q)
-                            if (oc + q < g.rows) row[oc + q] = elem<T>(y[m], q);
+                            if (oc + q < g.rows && oc + q >= lo) row[oc + q] = elem<T>(y[m], q);
                     }
                 }
             }
@@ -226,7 +308,7 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
 template <typename T, int MR, int MC, int NT, bool VI, bool SO, bool PF>
 cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
-    constexpr size_t smem = size_t(V * MR) * MC * 16;
+    constexpr size_t smem = size_t(V * MR + (SO ? V : 0)) * MC * 16;  // + halo rows
     auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
     // Resident blocks per SM on each device; 0 = not set up on that device yet.
     static std::atomic<int> resident[64];

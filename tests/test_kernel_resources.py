@@ -64,8 +64,11 @@ def test_default_bf16_vector_tile_budget(vec_report):
 
 
 def test_shifted_store_tile_budget(vec_report):
+    # 64 registers keep 4 blocks of 256 threads per SM
     k = _find(vec_report, "k_tile_vecIjLi32ELi16ELi256ELb1ELb1ELb0E")  # C3's 128x64 tile
-    assert k["regs"] <= 72 and k["spill"] == 0
+    assert k["regs"] <= 64 and k["spill"] == 0
+    k = _find(vec_report, "k_tile_vecItLi16ELi16ELi256ELb1ELb1ELb0E")  # bf16 128x128, shifted
+    assert k["regs"] <= 88 and k["spill"] == 0
 
 
 @pytest.mark.parametrize("src", ["tile_tma.cu", "inplace.cu", "copy.cu", "tile_lsu.cu"])
