@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
                 if (!full && orow >= g.n) break;
                 T *row = plane + orow * g.ld;
                 if (VEC && (full || oc + V <= g.n)) {
-                    *reinterpret_cast<uint4 *>(row + oc) = yv[m].v;
+                    __stcs(reinterpret_cast<uint4 *>(row + oc), yv[m].v);  // streaming store
                 } else {
 #pragma unroll
                     for (int q = 0; q < V; ++q)
