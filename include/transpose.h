@@ -48,6 +48,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* The library is built with hidden symbol visibility; the declarations below
+ * are the only symbols it exports. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -261,6 +267,10 @@ int32_t tr_version(void);
 
 #ifdef __cplusplus
 }
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
 #endif
 
 #endif /* LIBTRANSPOSE_TRANSPOSE_H */

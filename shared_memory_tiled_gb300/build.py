@@ -24,6 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "-Xcompiler", "-fvisibility=hidden",  # only the header's tr_* entry points are exported
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["api.cu", "copy.cu", "tile_lsu.cu", "tile_vec.cu", "tile_vec_u32.cu",
            "tile_vec_u32_prefetch.cu", "tile_vec_u16.cu", "tile_vec_u16_prefetch.cu",

@@ -46,6 +46,17 @@ def test_exports_are_c_linkage(lib):
     assert set(declared_functions()) <= exported
 
 
+def test_only_the_declared_entry_points_are_exported(lib):
+    """Everything else is hidden, so a second copy of the library (or any other
+    library) in the same process shares none of its kernels or caches."""
+    import shutil
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read()
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert names == set(declared_functions()), sorted(names - set(declared_functions()))
+
+
 def test_version_and_strings(lib):
     assert B.tr_version() == 10000
     for s in B.Status:
