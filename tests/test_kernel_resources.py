@@ -71,6 +71,14 @@ def test_shifted_store_tile_budget(vec_report):
     assert k["regs"] <= 88 and k["spill"] == 0
 
 
+def test_inplace_budgets():
+    # fp32: both tiles' loads in flight, 4 blocks/SM; bf16: staged one tile
+    # after the other, 3 blocks/SM (64 KiB of shared memory each)
+    rep = ptxas_report("inplace.cu")
+    assert _find(rep, "k_inplaceIjLb1E")["regs"] <= 64
+    assert _find(rep, "k_inplaceItLb1E")["regs"] <= 80
+
+
 @pytest.mark.parametrize("src", ["tile_tma.cu", "inplace.cu", "copy.cu", "tile_lsu.cu"])
 def test_no_spills(src):
     for name, k in ptxas_report(src).items():
