@@ -2,11 +2,10 @@
 //
 // The out-of-place kernels read one tile and write its transpose elsewhere.
 // In place, the transpose of tile (ti, tj) lands where tile (tj, ti) lives, so
-// one block owns each unordered pair of tiles: it reads BOTH tiles into
-// registers, stages them in two swizzled shared tiles, and only after the
-// barrier writes each one's transpose over the other ("Shared memory and the
-// bank conflict", "The barrier": nothing may be written before every thread's
-// reads are in).  A diagonal tile is its own partner.  No other block reads or
+// one block owns each unordered pair of tiles: it reads BOTH tiles (through
+// registers) into two swizzled shared tiles, and only after the barrier writes
+// each one's transpose over the other ("Shared memory and the bank conflict",
+// "The barrier": nothing may be written before every thread's reads are in).  A diagonal tile is its own partner.  No other block reads or
 // writes either tile, so blocks never race.
 //
 // Layout and lane mapping are those of the vectorised swizzled tile
