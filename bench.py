@@ -436,7 +436,8 @@ def run_ours(args):
     c_total = max_over_ranks(c_total, world)
     copy_gbs = 2 * copy_bytes * args.steps / (c_total / 1e3) / 1e9
     # context: torch's own device copy of the same bytes, timed the same way
-    tc_total = timed(lambda: c_out.copy_(c_in), args.steps, args.warmup)
+    tc_total = (timed_flushed if flush_l2 else timed)(lambda: c_out.copy_(c_in), args.steps,
+                                                      args.warmup)
     tc_total = max_over_ranks(tc_total, world)
     torch_copy_gbs = 2 * copy_bytes * args.steps / (tc_total / 1e3) / 1e9
 

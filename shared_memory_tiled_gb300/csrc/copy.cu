@@ -3,6 +3,7 @@
 // section "What to record": the transpose sits next to a copy of the same
 // bytes).  Moving N bytes costs N bytes read plus N bytes written, exactly the
 // algorithmic traffic of a transpose of N bytes.
+#include "launch.cuh"
 #include "tr_internal.h"
 
 namespace tr {
@@ -18,6 +19,7 @@ constexpr int kUnroll = 4;  // 16-byte vectors in flight per thread
 __global__ void __launch_bounds__(kThreads)
 k_copy_aligned(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int head,
                int64_t n16, int tail) {
+    pdl_prologue();
     if (blockIdx.x == 0) {
         if (threadIdx.x < head) out[threadIdx.x] = in[threadIdx.x];
         const int64_t t0 = head + n16 * 16;
@@ -55,6 +57,7 @@ template <typename W>
 __global__ void __launch_bounds__(kThreads)
 k_copy_narrow(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int head, int64_t nw,
               int tail) {
+    pdl_prologue();
     if (blockIdx.x == 0) {
         if (threadIdx.x < head) out[threadIdx.x] = in[threadIdx.x];
         const int64_t t0 = head + nw * int64_t(sizeof(W));
@@ -87,19 +90,18 @@ cudaError_t launch_copy(const void *in_, void *out_, size_t bytes, cudaStream_t 
         const int64_t n16 = (n - head) / 16;
         const int tail = int(n - head - n16 * 16);
         const int64_t grid = grid_for(n16, int64_t(kThreads) * kUnroll);
-        k_copy_aligned<<<unsigned(grid), kThreads, 0, stream>>>(in, out, head, n16, tail);
+        return launch_pdl(k_copy_aligned, dim3(unsigned(grid)), dim3(kThreads), 0, stream, in, out,
+                          head, n16, tail);
     } else if (((a ^ b) & 3u) == 0) {
         int head = int((4 - (a & 3u)) & 3u);
         if (head > n) head = int(n);
         const int64_t nw = (n - head) / 4;
         const int tail = int(n - head - nw * 4);
-        k_copy_narrow<uint32_t><<<unsigned(grid_for(nw, kThreads)), kThreads, 0, stream>>>(
-            in, out, head, nw, tail);
-    } else {
-        k_copy_narrow<uint8_t><<<unsigned(grid_for(n, kThreads)), kThreads, 0, stream>>>(
-            in, out, 0, n, 0);
+        return launch_pdl(k_copy_narrow<uint32_t>, dim3(unsigned(grid_for(nw, kThreads))),
+                          dim3(kThreads), 0, stream, in, out, head, nw, tail);
     }
-    return cudaGetLastError();
+    return launch_pdl(k_copy_narrow<uint8_t>, dim3(unsigned(grid_for(n, kThreads))), dim3(kThreads),
+                      0, stream, in, out, 0, n, 0);
 }
 
 }  // namespace tr

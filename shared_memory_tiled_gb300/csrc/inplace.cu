@@ -16,6 +16,7 @@
 //
 // Blocks walk a batch * T * T grid of tile coordinates (T tiles per side) and
 // skip the lower triangle, so each pair is taken exactly once.
+#include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
 #include "vec_common.cuh"
@@ -39,6 +40,7 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
     constexpr int LOADS = V;        // 16 tile rows per load pass, TILE rows
     extern __shared__ uint4 smem[]; // two tiles of TILE rows x 16 chunks
     uint4 *tile0 = smem, *tile1 = smem + TILE * 16;
+    pdl_prologue();
 
     const int t = threadIdx.x;
     const int lcc = t & 15, lr = t >> 4;  // phase 1: chunk and first row
@@ -164,8 +166,7 @@ cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
             }
         }
     }
-    kern<<<grid_blocks(g.total), 256, smem, stream>>>(data, g);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid_blocks(g.total)), dim3(256), smem, stream, data, g);
 }
 
 }  // namespace

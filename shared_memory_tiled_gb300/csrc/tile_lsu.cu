@@ -6,6 +6,7 @@
 // All index arithmetic is 64-bit; tiles are walked through a 1-D grid whose
 // block index is split into (plane, tile row, tile column), tile column
 // fastest, with a grid-stride loop for problems beyond the grid limit.
+#include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
 
@@ -22,6 +23,7 @@ namespace {
 template <typename T, bool READ_ROWS>
 __global__ void __launch_bounds__(256) k_naive(const T *__restrict__ in, T *__restrict__ out,
                                                Geometry g) {
+    pdl_prologue();
     for (int64_t t = blockIdx.x; t < g.total; t += gridDim.x) {
         int64_t b, tr, tc;
         split_tile(g, t, false, b, tr, tc);
@@ -61,6 +63,7 @@ template <typename T, int PAD>
 __global__ void __launch_bounds__(256) k_tile_pad(const T *__restrict__ in, T *__restrict__ out,
                                                   Geometry g) {
     __shared__ T tile[32][32 + PAD];
+    pdl_prologue();
     const int tx = threadIdx.x, ty = threadIdx.y;
     for (int64_t t = blockIdx.x; t < g.total; t += gridDim.x) {
         int64_t b, tr, tc;
@@ -84,24 +87,23 @@ __global__ void __launch_bounds__(256) k_tile_pad(const T *__restrict__ in, T *_
 }
 
 template <typename T, int PAD>
-void launch_pad_one(const Problem &p, const Geometry &g) {
-    k_tile_pad<T, PAD><<<grid_blocks(g.total), dim3(32, 8), 0, p.stream>>>(
-        static_cast<const T *>(p.in), static_cast<T *>(p.out), g);
+cudaError_t launch_pad_one(const Problem &p, const Geometry &g) {
+    return launch_pdl(k_tile_pad<T, PAD>, dim3(grid_blocks(g.total)), dim3(32, 8), 0, p.stream,
+                      static_cast<const T *>(p.in), static_cast<T *>(p.out), g);
 }
 
 template <typename T>
 cudaError_t launch_pad_typed(const Problem &p, int pad) {
     const Geometry g = make_geometry(p, 32, 32);
     switch (pad) {
-        case 0: launch_pad_one<T, 0>(p, g); break;
-        case 1: launch_pad_one<T, 1>(p, g); break;
-        case 2: launch_pad_one<T, 2>(p, g); break;
-        case 3: launch_pad_one<T, 3>(p, g); break;
-        case 4: launch_pad_one<T, 4>(p, g); break;
-        case 8: launch_pad_one<T, 8>(p, g); break;
+        case 0: return launch_pad_one<T, 0>(p, g);
+        case 1: return launch_pad_one<T, 1>(p, g);
+        case 2: return launch_pad_one<T, 2>(p, g);
+        case 3: return launch_pad_one<T, 3>(p, g);
+        case 4: return launch_pad_one<T, 4>(p, g);
+        case 8: return launch_pad_one<T, 8>(p, g);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template <typename T>
@@ -110,10 +112,10 @@ cudaError_t launch_naive_typed(const Problem &p, bool read_rows) {
     const T *in = static_cast<const T *>(p.in);
     T *out = static_cast<T *>(p.out);
     if (read_rows)
-        k_naive<T, true><<<grid_blocks(g.total), dim3(32, 8), 0, p.stream>>>(in, out, g);
-    else
-        k_naive<T, false><<<grid_blocks(g.total), dim3(32, 8), 0, p.stream>>>(in, out, g);
-    return cudaGetLastError();
+        return launch_pdl(k_naive<T, true>, dim3(grid_blocks(g.total)), dim3(32, 8), 0, p.stream,
+                          in, out, g);
+    return launch_pdl(k_naive<T, false>, dim3(grid_blocks(g.total)), dim3(32, 8), 0, p.stream, in,
+                      out, g);
 }
 
 }  // namespace

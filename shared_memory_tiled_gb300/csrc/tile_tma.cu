@@ -42,6 +42,7 @@
 // micro-block with bounds-checked element stores.  Input rows need no such
 // care: extra elements a load brings in land in output rows past `cols`, which
 // the store clips (whole lines).
+#include "launch.cuh"
 #include "ptx.cuh"
 #include "tr_internal.h"
 
@@ -130,6 +131,7 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
     using L = TmaTile<T>;
     constexpr int V = L::V;
     extern __shared__ uint8_t smem_raw[];
+    pdl_prologue();
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *in_buf = base;
@@ -279,6 +281,7 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
     using L = WarpTile<T>;
     constexpr int V = L::V;
     extern __shared__ uint8_t smem_raw[];
+    pdl_prologue();
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -429,6 +432,7 @@ k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
     using L = WarpTile<T>;
     constexpr int V = L::V;
     extern __shared__ uint8_t smem_raw[];
+    pdl_prologue();
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -563,6 +567,7 @@ k_tma_ws(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
     using L = TmaTile<T>;
     constexpr int V = L::V;
     extern __shared__ uint8_t smem_raw[];
+    pdl_prologue();
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = g.in_stages;
@@ -890,15 +895,15 @@ cudaError_t launch_typed(const Problem &p, const TmaConfig &cfg, const char **wh
     const int64_t units = cta_tile ? g.total : (g.total + kWarpsPerBlock - 1) / kWarpsPerBlock;
     int64_t grid = int64_t(dev.sms) * per_sm;
     if (grid > units) grid = units;
+    const dim3 gd{unsigned(grid)};
     if (kind == kPerWarp)
-        k_tma_warp<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, tm_out, g);
-    else if (kind == kLoadOnly)
-        k_tma_ldst<T><<<unsigned(grid), 32 * kWarpsPerBlock, smem, p.stream>>>(tm_in, g);
-    else if (kind == kWarpSpec)
-        k_tma_ws<T><<<unsigned(grid), kWsThreads, smem, p.stream>>>(tm_in, g);
-    else
-        k_tma<T><<<unsigned(grid), kThreads, smem, p.stream>>>(tm_in, tm_out, g);
-    return cudaGetLastError();
+        return launch_pdl(k_tma_warp<T>, gd, dim3(32 * kWarpsPerBlock), smem, p.stream, tm_in,
+                          tm_out, g);
+    if (kind == kLoadOnly)
+        return launch_pdl(k_tma_ldst<T>, gd, dim3(32 * kWarpsPerBlock), smem, p.stream, tm_in, g);
+    if (kind == kWarpSpec)
+        return launch_pdl(k_tma_ws<T>, gd, dim3(kWsThreads), smem, p.stream, tm_in, g);
+    return launch_pdl(k_tma<T>, gd, dim3(kThreads), smem, p.stream, tm_in, tm_out, g);
 }
 
 }  // namespace

@@ -49,6 +49,7 @@
 // missing.
 #pragma once
 
+#include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
 #include "vec_common.cuh"
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     constexpr int HL = SHIFT_OUT ? (HCH + NT - 1) / NT : 1;  // halo chunks per thread
     extern __shared__ uint4 smem[];          // TR + HALO rows of MC chunks
 
+    pdl_prologue();
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
 
@@ -339,9 +341,8 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
         const int64_t cap = int64_t(sm_count()) * fit;
         if (grid > cap) grid = cap;
     }
-    kern<<<grid_blocks(grid), NT, smem, p.stream>>>(static_cast<const T *>(p.in),
-                                                     static_cast<T *>(p.out), g, diagonal);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid_blocks(grid)), dim3(NT), smem, p.stream,
+                      static_cast<const T *>(p.in), static_cast<T *>(p.out), g, diagonal);
 }
 
 template <typename T, int MR, int MC, int NT, bool PF>

@@ -44,7 +44,7 @@ struct VecConfig {
     int tile_rows;     // tile shape in elements, 0 = default
     int tile_cols;
     bool prefetch;     // persistent blocks that prefetch their next tile
-    int threads;       // threads per block (128 or 256), 0 = default
+    int threads;       // threads per block (32, 64, 128 or 256), 0 = default
 };
 
 // Launchers: each returns the CUDA error of the launch (cudaSuccess when fine).
