@@ -30,6 +30,14 @@
  *     allocates no device memory in any call.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and do not synchronize.
+ *   - The transpose and copy kernels are launched with programmatic stream
+ *     serialization: one may be scheduled while the previous kernel in the
+ *     stream is still draining, and it waits for that kernel to complete
+ *     before touching memory, so results follow plain stream order.  They
+ *     signal their dependents at start, so a kernel that the caller launches
+ *     after them WITH programmatic stream serialization must itself wait
+ *     (cudaGridDependencySynchronize) before reading their output; kernels
+ *     launched without it are ordered as usual.
  *   - A zero dimension returns TR_OK without launching anything.  A negative
  *     dimension returns TR_ERR_BAD_DIM, a pitch below its minimum
  *     TR_ERR_BAD_LD, a NULL pointer with a nonzero size TR_ERR_NULL, and any
