@@ -67,3 +67,23 @@ def test_chain_through_copy_inplace_and_a_torch_kernel():
     torch.cuda.synchronize()
     assert torch.equal(a, ref + 10)
     assert torch.equal(b, ref + 9)
+
+
+def test_every_pair_of_kernels_back_to_back():
+    """A -> B with one variant, B -> A with another, for every ordered pair:
+    persistent TMA grids followed by one-tile-per-block grids and back."""
+    import torch
+    rows, cols = 1536, 2048 + 64
+    a = torch.randint(-2**31, 2**31 - 1, (rows * cols,), dtype=torch.int32, device="cuda")
+    ref = a.clone()
+    b = torch.empty_like(a)
+    fwd = B.make_args(a.data_ptr(), b.data_ptr(), B.DType.F32, 1, rows, cols, cols, rows)
+    bwd = B.make_args(b.data_ptr(), a.data_ptr(), B.DType.F32, 1, cols, rows, rows, cols)
+    opts = [B.make_options(**kw) for kw in KINDS]
+    for o1 in opts:
+        for o2 in opts:
+            B.check(B.tr_transpose_ex(fwd, o1))
+            B.check(B.tr_transpose_ex(bwd, o2))
+    torch.cuda.synchronize()
+    assert torch.equal(a, ref)
+    assert torch.equal(b.view(cols, rows), ref.view(rows, cols).t())
