@@ -45,6 +45,7 @@
 #include "launch.cuh"
 #include "ptx.cuh"
 #include "tr_internal.h"
+#include "vec_common.cuh"
 
 #include <atomic>
 #include <cstdio>
@@ -98,30 +99,6 @@ __device__ __forceinline__ void tile_coords(const TmaGeom &g, int64_t t, int32_t
     b = int32_t(bb);
     tr = int32_t(r_);
     tc = int32_t(c_);
-}
-
-__device__ __forceinline__ void micro_transpose(const uint4 (&x)[4], uint4 (&y)[4]) {
-    y[0] = make_uint4(x[0].x, x[1].x, x[2].x, x[3].x);
-    y[1] = make_uint4(x[0].y, x[1].y, x[2].y, x[3].y);
-    y[2] = make_uint4(x[0].z, x[1].z, x[2].z, x[3].z);
-    y[3] = make_uint4(x[0].w, x[1].w, x[2].w, x[3].w);
-}
-
-// 8x8 transpose of 16-bit elements: output row m takes half (m & 1) of word
-// (m >> 1) of every input row; output word w pairs input rows 2w and 2w+1.
-__device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
-    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ void micro_transpose(const uint4 (&x)[8], uint4 (&y)[8]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const unsigned sel = (m & 1) ? 0x7632u : 0x5410u;
-        const int k = m >> 1;
-        y[m] = make_uint4(__byte_perm(word_of(x[0], k), word_of(x[1], k), sel),
-                          __byte_perm(word_of(x[2], k), word_of(x[3], k), sel),
-                          __byte_perm(word_of(x[4], k), word_of(x[5], k), sel),
-                          __byte_perm(word_of(x[6], k), word_of(x[7], k), sel));
-    }
 }
 
 template <typename T>
@@ -189,13 +166,13 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
 
         const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
         uint8_t *ob = out_buf + size_t(k % SO) * L::BUF_BYTES;
-        uint4 x[V], y[V];
+        Chunk x[V], y[V];
 #pragma unroll
-        for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
+        for (int m = 0; m < V; ++m) x[m].v = *reinterpret_cast<const uint4 *>(ib + roff[m]);
         micro_transpose(x, y);
         if (!direct) {
 #pragma unroll
-            for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[m]) = y[m];
+            for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[m]) = y[m].v;
             ptx::fence_proxy_async_smem();
         } else if (ok) {
             // Last tile row of a ragged output: bounds-checked element stores.
@@ -205,15 +182,9 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
             for (int m = 0; m < V; ++m) {
                 const int64_t orow = int64_t(tc) * L::TILE + V * C + m;
                 if (orow < g.cols) {
-                    const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        if (oc + e < g.rows) {
-                            const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
-                            dst[orow * g.ld_out + oc + e] =
-                                T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
-                        }
-                    }
+                    for (int e = 0; e < V; ++e)
+                        if (oc + e < g.rows) dst[orow * g.ld_out + oc + e] = elem<T>(y[m], e);
                 }
             }
         }
@@ -343,13 +314,13 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
         uint8_t *ob = out_buf + size_t(k % SO) * L::BYTES;
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            uint4 xv[V], yv[V];
+            Chunk xv[V], yv[V];
 #pragma unroll
-            for (int m = 0; m < V; ++m) xv[m] = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
+            for (int m = 0; m < V; ++m) xv[m].v = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
             micro_transpose(xv, yv);
             if (!direct) {
 #pragma unroll
-                for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[p][m]) = yv[m];
+                for (int m = 0; m < V; ++m) *reinterpret_cast<uint4 *>(ob + woff[p][m]) = yv[m].v;
             } else {
                 // Last tile row of a ragged output: bounds-checked element stores.
                 T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
@@ -358,15 +329,9 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
                 for (int m = 0; m < V; ++m) {
                     const int64_t orow = int64_t(tc) * L::TILE + V * x + m;
                     if (orow < g.cols) {
-                        const uint32_t wv[4] = {yv[m].x, yv[m].y, yv[m].z, yv[m].w};
 #pragma unroll
-                        for (int e = 0; e < V; ++e) {
-                            if (oc + e < g.rows) {
-                                const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
-                                dst[orow * g.ld_out + oc + e] =
-                                    T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
-                            }
-                        }
+                        for (int e = 0; e < V; ++e)
+                            if (oc + e < g.rows) dst[orow * g.ld_out + oc + e] = elem<T>(yv[m], e);
                     }
                 }
             }
@@ -412,9 +377,9 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
 // (bf16), which makes (row % 8) distinct across the 8 lanes at every step; the
 // rotation is undone in registers before the micro-transpose.
 template <int V>
-__device__ __forceinline__ void unrotate(uint4 (&x)[V], int rot) {
+__device__ __forceinline__ void unrotate(Chunk (&x)[V], int rot) {
     // x[m] holds row (m + rot) % V; afterwards x[j] holds row j.
-    uint4 t[V];
+    Chunk t[V];
 #pragma unroll
     for (int step = 1; step < V; step <<= 1) {
         if (rot & step) {
@@ -485,11 +450,11 @@ k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
         int32_t b, tr, tc;
         tile_coords(g, gw + k * G, b, tr, tc);
         const uint8_t *ib = in_buf + size_t(slot) * L::BYTES;
-        uint4 x[2][V];
+        Chunk x[2][V];
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
-            for (int m = 0; m < V; ++m) x[p][m] = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
+            for (int m = 0; m < V; ++m) x[p][m].v = *reinterpret_cast<const uint4 *>(ib + roff[p][m]);
         __syncwarp();  // the slot is read: it may be refilled
         if (lane == 0 && k + S < n_local) issue_load(k + S, slot);
 
@@ -501,25 +466,21 @@ k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
         for (int p = 0; p < 2; ++p) {
             const int C = 4 * p + (lane >> 3);
             unrotate<V>(x[p], rot);
-            uint4 y[V];
+            Chunk y[V];
             micro_transpose(x[p], y);
 #pragma unroll
             for (int m = 0; m < V; ++m) {
                 const int64_t orow = c0 + V * C + m;
                 T *row = dst + orow * g.ld_out;
                 if (full_tile) {
-                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
                 } else if (orow < g.cols) {
                     if (oc + V <= g.rows) {
-                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
                     } else {
-                        const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
 #pragma unroll
                         for (int e = 0; e < V; ++e)
-                            if (oc + e < g.rows) {
-                                const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
-                                row[oc + e] = T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
-                            }
+                            if (oc + e < g.rows) row[oc + e] = elem<T>(y[m], e);
                     }
                 }
             }
@@ -636,16 +597,16 @@ k_tma_ws(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
             break;
         }
         const uint8_t *ib = in_buf + size_t(slot) * L::BUF_BYTES;
-        uint4 x[V];
+        Chunk x[V];
 #pragma unroll
-        for (int m = 0; m < V; ++m) x[m] = *reinterpret_cast<const uint4 *>(ib + roff[m]);
+        for (int m = 0; m < V; ++m) x[m].v = *reinterpret_cast<const uint4 *>(ib + roff[m]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + slot);
 
         int32_t b, tr, tc;
         tile_coords(g, int64_t(blockIdx.x) + k * gridDim.x, b, tr, tc);
         unrotate<V>(x, rot);
-        uint4 y[V];
+        Chunk y[V];
         micro_transpose(x, y);
         T *dst = static_cast<T *>(g.out) + int64_t(b) * g.stride_out;
         const int64_t r0 = int64_t(tr) * L::TILE, c0 = int64_t(tc) * L::TILE;
@@ -656,18 +617,14 @@ k_tma_ws(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
             const int64_t orow = c0 + V * C + m;
             T *row = dst + orow * g.ld_out;
             if (full_tile) {
-                __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
             } else if (orow < g.cols) {
                 if (oc + V <= g.rows) {
-                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m]);
+                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
                 } else {
-                    const uint32_t wv[4] = {y[m].x, y[m].y, y[m].z, y[m].w};
 #pragma unroll
                     for (int e = 0; e < V; ++e)
-                        if (oc + e < g.rows) {
-                            const uint32_t word = wv[sizeof(T) == 4 ? e : e >> 1];
-                            row[oc + e] = T(sizeof(T) == 4 ? word : (word >> ((e & 1) * 16)));
-                        }
+                        if (oc + e < g.rows) row[oc + e] = elem<T>(y[m], e);
                 }
             }
         }
