@@ -442,16 +442,18 @@ def run_ours(args):
     torch_copy_gbs = 2 * copy_bytes * args.steps / (tc_total / 1e3) / 1e9
 
     # ---- end to end: pinned host input -> device -> transpose -> pinned host output.
-    # Steps alternate between two streams with their own device and pinned
-    # output buffers, so the device->host copy of one step overlaps the
+    # Steps rotate over `e2e_streams` streams, each with its own device and
+    # pinned output buffers, so the device->host copy of one step overlaps the
     # host->device copy of the next (the link carries both directions at once);
     # within a step the three operations stay ordered on its stream.
     k_e2e = max(3, min(args.steps, 20))
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    d_in2 = torch.empty_like(d_in)
-    d_out2 = d_in2 if inplace else torch.empty_like(d_out)
-    pins_out = [pin_out, torch.empty_like(pin_out).pin_memory()]
-    bufs = [(d_in, d_in if inplace else d_out), (d_in2, d_out2)]
+    ns = max(2, args.e2e_streams)
+    streams = [torch.cuda.Stream(dev) for _ in range(ns)]
+    pins_out = [pin_out] + [torch.empty_like(pin_out).pin_memory() for _ in range(ns - 1)]
+    bufs = [(d_in, d_in if inplace else d_out)]
+    for _ in range(ns - 1):
+        di = torch.empty_like(d_in)
+        bufs.append((di, di if inplace else torch.empty_like(d_out)))
     e_args = []
     for i, st in enumerate(streams):
         di, do = bufs[i]
@@ -474,26 +476,28 @@ def run_ours(args):
 
     def e2e_run(k):
         for j in range(k):
-            e2e_step_on(j % 2)
+            e2e_step_on(j % ns)
 
-    e2e_run(2)  # warm-up
+    e2e_run(ns)  # warm-up
     torch.cuda.synchronize(dev)
     barrier(world)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(streams[0])
-    streams[1].wait_event(t0)
+    for st in streams[1:]:
+        st.wait_event(t0)
     e2e_run(k_e2e)
-    done1 = torch.cuda.Event()
-    done1.record(streams[1])
-    streams[0].wait_event(done1)
+    for st in streams[1:]:
+        done = torch.cuda.Event()
+        done.record(st)
+        streams[0].wait_event(done)
     t1.record(streams[0])
     torch.cuda.synchronize(dev)
     barrier(world)
     e_total = max_over_ranks(t0.elapsed_time(t1), world)
     e2e_gbs = w.algorithmic_bytes * k_e2e * world / (e_total / 1e3) / 1e9
     # every end-to-end step uploads the input and transposes it once
-    e2e_got = pins_out[(k_e2e - 1) % 2].numpy().view(x_host.dtype)
+    e2e_got = pins_out[(k_e2e - 1) % ns].numpy().view(x_host.dtype)
     e2e_dst = (e2e_got[jj * w.ld_in + ii] if inplace
                else e2e_got[bb * w.sout + jj * w.ld_out + ii])
     if not np.array_equal(e2e_dst, src):
@@ -535,7 +539,8 @@ def run_ours(args):
                      "traffic": traffic, "peak_source": peak_kind, "kernel": kname,
                      "bytes_per_launch": w.algorithmic_bytes},
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "steps": k_e2e,
-                "overlap": "two streams: one step's device->host copy runs with the next one's host->device copy",
+                "overlap": (f"{ns} streams: one step's device->host copy runs with the next one's "
+                            "host->device copy"),
                 "h2d_bytes_per_step": w.in_elems * w.esize,
                 "d2h_bytes_per_step": w.out_elems * w.esize},
         "gpu_launches": args.steps,
@@ -585,6 +590,8 @@ def main(argv=None):
                     help="vector tile: 1 = one tile per block, 2 = persistent with prefetch")
     ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    ap.add_argument("--e2e-streams", dest="e2e_streams", type=int, default=3,
+                    help="streams (and buffer sets) the end-to-end steps rotate over")
     ap.add_argument("--clock-window", dest="clock_window", type=float, default=1.0,
                     help="seconds of untimed re-runs for clock sampling when the timed "
                          "region is shorter than this (0 = none)")
