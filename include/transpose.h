@@ -38,6 +38,9 @@
  *     after them WITH programmatic stream serialization must itself wait
  *     (cudaGridDependencySynchronize) before reading their output; kernels
  *     launched without it are ordered as usual.
+ *   - Calls can be captured into a CUDA graph and replayed.  The first call
+ *     of a configuration on a device sets kernel attributes (shared-memory
+ *     limits, occupancy), so make it once before capturing.
  *   - A zero dimension returns TR_OK without launching anything.  A negative
  *     dimension returns TR_ERR_BAD_DIM, a pitch below its minimum
  *     TR_ERR_BAD_LD, a NULL pointer with a nonzero size TR_ERR_NULL, and any
