@@ -78,3 +78,27 @@ def test_inplace_beyond_2_31_elements():
     assert torch.equal(v[:, -3:], ref[1].t())
     del x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("ld_in,ld_out", [(32804, 65539), (32803, 65540)],
+                         ids=["odd-output-pitch", "odd-input-pitch"])
+def test_fp32_misaligned_pitches_beyond_2_31_elements(ld_in, ld_out):
+    """Past 2**31 elements with rows that start off 16-byte boundaries: the
+    shifted stores (with their halo rows) on the output side, single-element
+    loads on the input side."""
+    import torch
+    rows, cols = 65537, 32801          # 2,149,679,137 elements
+    x = torch.randint(-2**31, 2**31 - 1, (rows * ld_in,), dtype=torch.int32, device="cuda")
+    out = torch.zeros(cols * ld_out, dtype=torch.int32, device="cuda")
+    args = B.make_args(x.data_ptr(), out.data_ptr(), B.DType.F32, 1, rows, cols, ld_in, ld_out)
+    B.check(B.tr_transpose_ex(args, B.make_options(B.Variant.AUTO)))
+    torch.cuda.synchronize()
+    _sampled_check(x, out, rows, cols, ld_in, ld_out, seed=3)
+    # every output row ends where it should: the element after it (pitch padding) is untouched
+    pad = out.view(cols, ld_out)[:, rows:]
+    assert int(torch.count_nonzero(pad)) == 0
+    xs = x.view(rows, ld_in)[:, :cols].to(torch.int64).sum()
+    os_ = out.view(cols, ld_out)[:, :rows].to(torch.int64).sum()
+    assert int(xs) == int(os_)
+    del x, out, pad
+    torch.cuda.empty_cache()
