@@ -49,9 +49,19 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
     bool first = true;
     for (int64_t w = blockIdx.x; w < g.total; w += gridDim.x) {
         const int64_t per_plane = g.tiles * g.tiles;
-        const int64_t b = w / per_plane;
-        const int64_t rem = w - b * per_plane;
-        const int64_t ti = rem / g.tiles, tj = rem - ti * g.tiles;
+        int64_t b, ti, tj;
+        if (g.total <= 0xFFFFFFFFll) {  // 32-bit division is far cheaper than 64-bit
+            const uint32_t w32 = uint32_t(w), pp = uint32_t(per_plane), t32 = uint32_t(g.tiles);
+            const uint32_t bb = w32 / pp, rem = w32 - bb * pp, i = rem / t32;
+            b = bb;
+            ti = i;
+            tj = rem - i * t32;
+        } else {
+            b = w / per_plane;
+            const int64_t rem = w - b * per_plane;
+            ti = rem / g.tiles;
+            tj = rem - ti * g.tiles;
+        }
         if (ti > tj) continue;  // the pair is handled at (tj, ti)
         T *plane = data + b * g.stride;
         const bool diag = ti == tj;
