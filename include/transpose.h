@@ -119,8 +119,8 @@ typedef enum tr_variant {
  * bf16 64x64.  Other combinations return TR_ERR_UNSUPPORTED.  With
  * tile_rows = tile_cols = 0 the shape follows the alignment of the two sides:
  * 128 rows x 16 chunks (fp32 128x64, bf16 128x128) when output rows do not
- * start on 16-byte boundaries, 16 x 32 chunks (fp32 64x128, bf16 128x256) when
- * input rows do not, the 256-thread default otherwise. */
+ * start on 16-byte boundaries, 16 chunks x 128 elements (fp32 64x128, bf16
+ * 128x128) when input rows do not, the 256-thread default otherwise. */
 typedef struct tr_options {
     int32_t variant;      /* tr_variant                                                  */
     int32_t pad;          /* TILE_PAD: shared row pitch is 32 + pad elements, 0..8        */

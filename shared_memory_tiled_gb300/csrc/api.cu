@@ -121,9 +121,11 @@ int32_t choose(const Problem &p, const tr_options *o) {
 // chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s with
 // 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16 with
 // output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128.  A
-// misaligned input is read one element at a time, which wants tiles twice as
-// wide (7919x12289 with pitch 12289: 95.7% of the copy with 64x128 against
-// 88.6% with 64x64).
+// misaligned input is read with the widest loads each chunk's own address
+// allows and takes tiles 16 chunks tall and 128 elements wide: 7919x12289 fp32
+// with input pitch 12289 reaches 6751 GB/s with 64x128 against 5999 with
+// 64x64; 16384x16384 bf16 with input pitch 16385 4094 GB/s with 128x128
+// against 2919 with 128x256.
 void auto_vec_shape(const Problem &p, bool in16, bool out16, int *rows, int *cols) {
     const int v = 16 / p.esize;  // elements per 16-byte chunk
     if (!out16) {
@@ -131,7 +133,7 @@ void auto_vec_shape(const Problem &p, bool in16, bool out16, int *rows, int *col
         *cols = 16 * v;
     } else if (!in16) {
         *rows = 16 * v;
-        *cols = 32 * v;
+        *cols = 128;
     } else {
         *rows = *cols = 0;  // kernel default: 64x64 fp32, 128x128 bf16
     }

@@ -125,6 +125,27 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                 const int64_t gr = r0 + lr + RPP * k;
                 if (VEC_IN && gr < g.rows && gc + V <= g.cols) {
                     ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + gc));
+                } else if (!VEC_IN && gr < g.rows && gc + V <= g.cols) {
+                    // A whole chunk in range on a misaligned side (row starts
+                    // differ from row to row): the widest loads this chunk's
+                    // own address allows, touching only its own elements.
+                    const T *p = src + gr * g.ld_in + gc;
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+                    if ((a & 15u) == 0) {
+                        ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(p));
+                    } else if ((a & 7u) == 0) {
+                        const uint2 lo = __ldcs(reinterpret_cast<const uint2 *>(p));
+                        const uint2 hi = __ldcs(reinterpret_cast<const uint2 *>(p) + 1);
+                        ld[k].v = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    } else if (sizeof(T) == 4 || (a & 3u) == 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ld[k].w[q] = __ldcs(reinterpret_cast<const unsigned int *>(p) + q);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ld[k].w[q] = uint32_t(p[2 * q]) | (uint32_t(p[2 * q + 1]) << 16);
+                    }
                 } else {
                     T e[V];
 #pragma unroll
