@@ -404,6 +404,10 @@ def run_ours(args):
 
     # per-launch statistics from a separate pass with an event after every step
     per_ms = step_times(step, args.steps)
+    # the median of repeated runs: more passes of K back-to-back steps, each
+    # between two events like the timed region (not part of `value`)
+    rep_ms = [max_over_ranks((timed_flushed if flush_l2 else timed)(step, args.steps, 0), world)
+              for _ in range(args.repeats)]
     hot_ms = max_over_ranks(timed(step, args.steps, args.warmup), world) if flush_l2 else None
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
@@ -529,6 +533,11 @@ def run_ours(args):
         "pct_of_hbm_measured": round(100 * gbs / world / peak, 2),
         "pct_of_hbm_nominal": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_copy": round(100 * gbs / (copy_gbs * world), 2),
+        "repeats": {"n": len(rep_ms), "unit": "GB/s",
+                    "median": round(w.algorithmic_bytes * args.steps / (statistics.median(rep_ms) / 1e3) / 1e9, 2) if rep_ms else None,
+                    "min": round(w.algorithmic_bytes * args.steps / (max(rep_ms) / 1e3) / 1e9, 2) if rep_ms else None,
+                    "max": round(w.algorithmic_bytes * args.steps / (min(rep_ms) / 1e3) / 1e9, 2) if rep_ms else None,
+                    "pass": "further passes of K back-to-back steps between two events (not in value)"},
         "step_ms": {"median": round(med_ms, 5), "min": round(min(per_ms), 5),
                     "p90": round(sorted(per_ms)[int(0.9 * (len(per_ms) - 1))], 5),
                     "pass": "separate pass of K steps with an event after each (not in value)"},
@@ -590,6 +599,8 @@ def main(argv=None):
                     help="vector tile: 1 = one tile per block, 2 = persistent with prefetch")
     ap.add_argument("--cpu-seconds", dest="cpu_seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="extra passes of K steps whose median is reported beside the value")
     ap.add_argument("--e2e-streams", dest="e2e_streams", type=int, default=3,
                     help="streams (and buffer sets) the end-to-end steps rotate over")
     ap.add_argument("--clock-window", dest="clock_window", type=float, default=1.0,
