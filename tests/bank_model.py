@@ -115,6 +115,35 @@ def tma_write(warp, m, V=4):
     return out
 
 
+def ws_consumer_read(warp, m, V=4):
+    """Warp-specialised pipeline (k_tma_ws), consumer read m: thread t < 256 owns
+    micro-block (A, C) = (t % 16, t // 16) and reads tile row V*A + (m + rot) % V
+    with rot = (A // 2) % 4 (fp32) or A % 8 (bf16), chunk C of the two-box slot."""
+    box = 16 * V * 128
+    out = []
+    for lane in range(32):
+        t = warp * 32 + lane
+        A, C = t & 15, t >> 4
+        rot = ((A >> 1) & 3) if V == 4 else (A & 7)
+        r = V * A + ((m + rot) & (V - 1))
+        out.append((C >> 3) * box + r * 128 + (((C & 7) ^ (r & 7)) << 4))
+    return out
+
+
+def ldst_read(m, p, V=4):
+    """Per-warp load-only pipeline (k_tma_ldst), read m of pass p: lane owns
+    A = lane % 8, C = 4p + lane // 8 in one 8V-row box, row V*A + (m + rot) % V
+    with rot = A // 2 (fp32) or A (bf16)."""
+    out = []
+    for lane in range(32):
+        A = lane & 7
+        rot = (A >> 1) if V == 4 else A
+        C = 4 * p + (lane >> 3)
+        r = V * A + ((m + rot) & (V - 1))
+        out.append(r * 128 + ((C ^ (r & 7)) << 4))
+    return out
+
+
 # --- the transposed operand store of the padded SGEMM page --------------------------------
 
 def sgemm_as_store(BK, a_stride, j, offset=0):

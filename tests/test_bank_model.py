@@ -97,3 +97,24 @@ def test_tma_addresses_cover_each_box_chunk_once():
         writes = sorted(a for w in range(8) for m in range(V) for a in BM.tma_write(w, m, V))
         expect = list(range(0, 2 * 16 * V * 128, 16))
         assert reads == expect and writes == expect
+
+
+@pytest.mark.parametrize("V", [4, 8])
+def test_rotated_reads_of_the_register_store_pipelines_are_conflict_free(V):
+    """The warp-specialised and load-only TMA pipelines read rows in a per-lane
+    rotated order so the 8 lanes of each 16-byte phase hit 8 swizzle positions;
+    without the rotation the same reads would conflict."""
+    ws = [a for w in range(8) for m in range(V) for a in BM.ws_consumer_read(w, m, V)]
+    assert sorted(ws) == list(range(0, 2 * 16 * V * 128, 16))   # each slot chunk once
+    for w in range(8):
+        for m in range(V):
+            assert BM.conflict_degree(BM.ws_consumer_read(w, m, V), 16) == 1
+    ld = [a for m in range(V) for p in range(2) for a in BM.ldst_read(m, p, V)]
+    assert sorted(ld) == list(range(0, 8 * V * 128, 16))          # each box chunk once
+    for m in range(V):
+        for p in range(2):
+            assert BM.conflict_degree(BM.ldst_read(m, p, V), 16) == 1
+    # the unrotated order: lanes A = 0..7 of a phase read row V*A + m
+    plain = [(V * (lane & 7) + 0) * 128 + (((lane >> 3) ^ ((V * (lane & 7)) & 7)) << 4)
+             for lane in range(32)]
+    assert BM.conflict_degree(plain, 16) > 1
