@@ -32,7 +32,11 @@
 // ("Shared-memory tiling and bank conflicts": pad or swizzle tiles when column
 // access creates bank conflicts).
 //
-// Misaligned sides.  VEC_IN = false loads single elements (any pitch).  With
+// Misaligned sides.  With VEC_IN = false (input rows need not start on
+// 16-byte boundaries) each chunk whose elements are all in range is loaded
+// with the widest accesses its own address allows -- one 16-byte, two 8-byte
+// or four 4-byte loads, single elements for bf16 rows 2 bytes past a word --
+// and never a byte outside the chunk.  With
 // SHIFT_OUT the output rows need not start on 16-byte boundaries (e.g. a row
 // pitch of 12289 fp32).  For each output row, d is the number of elements
 // between the tile's first column r0 and the row's next 16-byte boundary (the
