@@ -27,7 +27,9 @@
  *   - Only the logical output elements are written; pitch padding of the
  *     output keeps whatever it held.
  *   - `in` and `out` are DEVICE pointers owned by the caller.  The library
- *     allocates no device memory in any call.
+ *     allocates no device memory in any call.  Each must sit on a boundary of
+ *     its element size (4 bytes for fp32, 2 for bf16), else the call returns
+ *     TR_ERR_UNSUPPORTED; beyond that any base address and pitch is accepted.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream) and do not synchronize.
  *   - The transpose and copy kernels are launched with programmatic stream
@@ -229,8 +231,8 @@ tr_status tr_copy(const void *in, void *out, size_t bytes, tr_stream_t stream);
  * element (k, m) at k*BM + m, i.e. out holds A[mt*BM + m][kt*BK + k].
  * BM in {64, 128}, BK in {8, 16, 32}, pad in 0..8 or negative for the page's
  * rule (32 / BK) % 8.  M and K must be multiples of BM and BK, `a` 16-byte
- * aligned and lda a multiple of 4 (float4 loads), else TR_ERR_UNSUPPORTED;
- * `out` (M*K words) must not overlap `a` (TR_ERR_OVERLAP).  Device pointers,
+ * aligned, lda a multiple of 4 (float4 loads) and `out` 4-byte aligned, else
+ * TR_ERR_UNSUPPORTED; `out` (M*K words) must not overlap `a` (TR_ERR_OVERLAP).  Device pointers,
  * caller-owned; asynchronous on `stream`. */
 tr_status tr_operand_tiles_f32(const float *a, float *out, int64_t m, int64_t k, int64_t lda,
                                int32_t bm, int32_t bk, int32_t pad, tr_stream_t stream);
@@ -245,7 +247,7 @@ tr_status tr_operand_tiles_f32(const float *a, float *out, int64_t m, int64_t k,
  *   layout 1: row pitch 33 (the padded tile, conflict-free)
  *   layout 2: pitch 32 with column index XOR row (swizzled, conflict-free)
  *   layout 3: pitch 32 read along rows, logical ((r + w) % 32, l) (reference)
- * `result` (device, blocks*256 words, caller-owned) receives each thread's
+ * `result` (device, blocks*256 words, 4-byte aligned, caller-owned) receives each thread's
  * fold, so the reads cannot be optimised away and the run is checkable.
  * Time it with events on `stream` to compare layouts. */
 tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *result,

@@ -58,6 +58,10 @@ tr_status validate(const tr_args *a, Problem *p, bool *empty) {
     *empty = a->batch == 0 || a->rows == 0 || a->cols == 0;
     if (*empty) return TR_OK;
     if (!a->in || !a->out) return TR_ERR_NULL;
+    // Every kernel accesses whole elements: a pointer off its element
+    // boundary would fault on the device.
+    if ((reinterpret_cast<uintptr_t>(a->in) | reinterpret_cast<uintptr_t>(a->out)) % esize)
+        return TR_ERR_UNSUPPORTED;
     if (a->ld_in < a->cols || a->ld_out < a->rows) return TR_ERR_BAD_LD;
     int64_t min_sin, min_sout;
     if (!mul_add(a->rows - 1, a->ld_in, a->cols, &min_sin) ||
@@ -220,6 +224,7 @@ tr_status run_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t l
     if (batch < 0 || n < 0) return TR_ERR_BAD_DIM;
     if (batch == 0 || n == 0) return TR_OK;
     if (!data) return TR_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(data) % esize) return TR_ERR_UNSUPPORTED;
     if (ld < n) return TR_ERR_BAD_LD;
     int64_t plane, ext, bytes;
     if (!mul_add(n - 1, ld, n, &plane)) return TR_ERR_BAD_DIM;
@@ -325,6 +330,7 @@ tr_status tr_operand_tiles_f32(const float *a, float *out, int64_t m, int64_t k,
     if (lda < k) return TR_ERR_BAD_LD;
     if (m % bm || k % bk) return TR_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(a) & 15u) || (lda & 3)) return TR_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(out) & 3u) return TR_ERR_UNSUPPORTED;
     int64_t ext_a, bytes_a, bytes_out;
     if (!tr::mul_add(m - 1, lda, k, &ext_a) || !tr::mul_add(ext_a, 4, 0, &bytes_a) ||
         !tr::mul_add(m, k * 4, 0, &bytes_out))
@@ -348,6 +354,7 @@ tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *
     if (reps < 0 || blocks < 0) return TR_ERR_BAD_DIM;
     if (blocks == 0) return TR_OK;
     if (!result) return TR_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(result) & 3u) return TR_ERR_UNSUPPORTED;
     const cudaError_t e = tr::launch_bank_probe(layout, reps, blocks, result,
                                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

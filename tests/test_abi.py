@@ -83,6 +83,11 @@ def test_single_matrix_argument_errors(lib, fn):
     assert f(FAKE_IN + 8, FAKE_IN, 4, 4, 4, 4) == B.Status.ERR_OVERLAP
     # overflowing extents
     assert f(FAKE_IN, FAKE_OUT, 1 << 40, 1 << 40, 1 << 40, 1 << 40) == B.Status.ERR_BAD_DIM
+    # a pointer off its element boundary is refused before any launch
+    es = 4 if fn.endswith("f32") else 2
+    for off in range(1, es):
+        assert f(FAKE_IN + off, FAKE_OUT, 4, 4, 4, 4) == B.Status.ERR_UNSUPPORTED
+        assert f(FAKE_IN, FAKE_OUT + off, 4, 4, 4, 4) == B.Status.ERR_UNSUPPORTED
     # empty problems succeed without touching anything, even with NULL pointers
     assert f(0, 0, 0, 5, 5, 0) == B.Status.OK
     assert f(0, 0, 7, 0, 0, 7) == B.Status.OK
@@ -173,6 +178,9 @@ def test_inplace_argument_errors(lib, fn):
     assert f(FAKE_IN, 1, 5, 4, 16) == B.Status.ERR_BAD_LD
     assert f(FAKE_IN, 2, 4, 4, 15) == B.Status.ERR_BAD_LD
     assert f(FAKE_IN, 1, 1 << 40, 1 << 40, 0) == B.Status.ERR_BAD_DIM
+    es = 4 if fn.endswith("f32") else 2
+    for off in range(1, es):
+        assert f(FAKE_IN + off, 1, 4, 4, 16) == B.Status.ERR_UNSUPPORTED
     assert f(0, 0, 4, 4, 16) == B.Status.OK and f(0, 3, 0, 0, 0) == B.Status.OK
 
 
@@ -185,6 +193,7 @@ def test_operand_tiles_argument_errors(lib):
     assert f(FAKE_IN, FAKE_OUT, 100, 16, 16, 128, 16) == B.Status.ERR_UNSUPPORTED
     assert f(FAKE_IN + 4, FAKE_OUT, 128, 16, 16, 128, 16) == B.Status.ERR_UNSUPPORTED
     assert f(FAKE_IN, FAKE_OUT, 128, 16, 18, 128, 16) == B.Status.ERR_UNSUPPORTED
+    assert f(FAKE_IN, FAKE_OUT + 2, 128, 16, 16, 128, 16) == B.Status.ERR_UNSUPPORTED
     assert f(FAKE_IN, FAKE_OUT, 128, 16, 8, 128, 16) == B.Status.ERR_BAD_LD
     assert f(0, FAKE_OUT, 128, 16, 16, 128, 16) == B.Status.ERR_NULL
     assert f(FAKE_IN, FAKE_IN + 64, 128, 16, 16, 128, 16) == B.Status.ERR_OVERLAP
@@ -195,6 +204,7 @@ def test_bank_probe_argument_errors(lib):
     assert B.tr_bank_probe(4, 1, 1, FAKE_OUT) == B.Status.ERR_UNSUPPORTED
     assert B.tr_bank_probe(0, -1, 1, FAKE_OUT) == B.Status.ERR_BAD_DIM
     assert B.tr_bank_probe(0, 1, 1, 0) == B.Status.ERR_NULL
+    assert B.tr_bank_probe(0, 1, 1, FAKE_OUT + 2) == B.Status.ERR_UNSUPPORTED
     assert B.tr_bank_probe(0, 1, 0, 0) == B.Status.OK
 
 
