@@ -120,9 +120,11 @@ typedef enum tr_variant {
  * threads (one warp, so the tile barrier is a warp barrier): fp32 32x32,
  * bf16 64x64.  Other combinations return TR_ERR_UNSUPPORTED.  With
  * tile_rows = tile_cols = 0 the shape follows the alignment of the two sides:
- * 128 rows x 16 chunks (fp32 128x64, bf16 128x128) when output rows do not
- * start on 16-byte boundaries, 16 chunks x 128 elements (fp32 64x128, bf16
- * 128x128) when input rows do not, the 256-thread default otherwise. */
+ * bf16 64x128 on 128 threads when input rows do not start on 16-byte
+ * boundaries (unless `threads` is set); else 128 rows x 16 chunks (fp32
+ * 128x64, bf16 128x128) when output rows do not; fp32 64x128 (bf16 128x128
+ * with `threads` set) when only input rows do not; the 256-thread default
+ * otherwise. */
 typedef struct tr_options {
     int32_t variant;      /* tr_variant                                                  */
     int32_t pad;          /* TILE_PAD: shared row pitch is 32 + pad elements, 0..8        */

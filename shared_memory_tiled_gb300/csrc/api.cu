@@ -111,8 +111,9 @@ bool options_valid(const tr_options *o) {
 // Variant choice (host logic only).  AUTO takes the vectorised swizzled tile,
 // the fastest variant measured on GB300 for every alignment class: it uses
 // 16-byte accesses on each side that allows them, realigns misaligned output
-// rows with warp shuffles, and loads single elements from a misaligned input.
-// TMA runs only when asked for.
+// rows with warp shuffles, and reads a misaligned input as aligned 16-byte
+// chunks realigned on chip (bf16) or with the widest loads each chunk's
+// address allows (fp32).  TMA runs only when asked for.
 int32_t choose(const Problem &p, const tr_options *o) {
     (void)p;
     const int req = o ? o->variant : TR_VARIANT_AUTO;
@@ -120,26 +121,33 @@ int32_t choose(const Problem &p, const tr_options *o) {
     return TR_VARIANT_TILE_VEC;
 }
 
-// Tile shape AUTO uses for the vectorised tile (measured on GB300).  Output
-// rows that are not 16-byte aligned (shifted stores) take 128-row tiles, 16
-// chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s with
-// 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16 with
-// output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128.  A
-// misaligned input is read with the widest loads each chunk's own address
-// allows and takes tiles 16 chunks tall and 128 elements wide: 7919x12289 fp32
-// with input pitch 12289 reaches 6751 GB/s with 64x128 against 5999 with
-// 64x64; 16384x16384 bf16 with input pitch 16385 4094 GB/s with 128x128
-// against 2919 with 128x256.
-void auto_vec_shape(const Problem &p, bool in16, bool out16, int *rows, int *cols) {
+// Tile shape (and, unless the caller chose one, block size) AUTO uses for the
+// vectorised tile (measured on GB300).  A misaligned bf16 input (aligned
+// chunks realigned on chip) takes 64x128 tiles on 128 threads: 16384x16384
+// bf16 with input pitch 16385 reaches 6598 GB/s, against 5961 with 128x128 on
+// 256 threads, 5848 with 128x128 on 128 and 5566 with 256x64 on 256; with the
+// output pitch odd as well, 4363 against 3661 with 128x128 on 256.  Otherwise
+// output rows that are not 16-byte aligned (shifted stores) take 128-row tiles,
+// 16 chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s
+// with 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16
+// with output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128.  A
+// misaligned fp32 input takes tiles 16 chunks tall and 128 elements wide:
+// 7919x12289 fp32 with input pitch 12289 reaches 6751 GB/s with 64x128
+// against 5999 with 64x64 and 5952 / 6171 with 128x64 / 64x64 on 128 threads.
+void auto_vec_shape(const Problem &p, bool in16, bool out16, VecConfig *cfg) {
     const int v = 16 / p.esize;  // elements per 16-byte chunk
-    if (!out16) {
-        *rows = 128;
-        *cols = 16 * v;
+    if (!in16 && p.esize == 2 && cfg->threads == 0) {
+        cfg->tile_rows = 64;
+        cfg->tile_cols = 128;
+        cfg->threads = 128;
+    } else if (!out16) {
+        cfg->tile_rows = 128;
+        cfg->tile_cols = 16 * v;
     } else if (!in16) {
-        *rows = 16 * v;
-        *cols = 128;
+        cfg->tile_rows = 16 * v;
+        cfg->tile_cols = 128;
     } else {
-        *rows = *cols = 0;  // kernel default: 64x64 fp32, 128x128 bf16
+        cfg->tile_rows = cfg->tile_cols = 0;  // kernel default: 64x64 fp32, 128x128 bf16
     }
 }
 
@@ -165,8 +173,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
             }
             VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
                           o && o->schedule == 2, o ? o->threads : 0};
-            if (cfg.tile_rows == 0 && cfg.tile_cols == 0)
-                auto_vec_shape(p, in16, out16, &cfg.tile_rows, &cfg.tile_cols);
+            if (cfg.tile_rows == 0 && cfg.tile_cols == 0) auto_vec_shape(p, in16, out16, &cfg);
             const char *why = nullptr;
             e = launch_tile_vec(p, in16, out16, cfg, &why);
             if (e != cudaSuccess && why) {

@@ -33,10 +33,12 @@
 // access creates bank conflicts).
 //
 // Misaligned sides.  With VEC_IN = false (input rows need not start on
-// 16-byte boundaries) each chunk whose elements are all in range is loaded
-// with the widest accesses its own address allows -- one 16-byte, two 8-byte
-// or four 4-byte loads, single elements for bf16 rows 2 bytes past a word --
-// and never a byte outside the chunk.  With
+// 16-byte boundaries) bf16 tiles that lie wholly inside the matrix read every
+// row segment as the aligned 16-byte chunks covering it, stage them unshifted
+// in shared memory and cut each thread's chunk out of two neighbours; all
+// other chunks whose elements are in range (fp32, edge tiles) are loaded with
+// the widest accesses their own address allows -- one 16-byte, two 8-byte or
+// four 4-byte loads, single elements for bf16 rows 2 bytes past a word.  With
 // SHIFT_OUT the output rows need not start on 16-byte boundaries (e.g. a row
 // pitch of 12289 fp32).  For each output row, d is the number of elements
 // between the tile's first column r0 and the row's next 16-byte boundary (the
@@ -64,7 +66,7 @@
 namespace tr {
 namespace vec {
 
-// Elements d .. d+V-1 of the 2V-element sequence (own, next), 0 < d < V.
+// Elements d .. d+V-1 of the 2V-element sequence (own, next), 0 <= d < V.
 template <typename T>
 __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int d) {
     uint32_t e[8] = {own.w[0], own.w[1], own.w[2], own.w[3],
@@ -86,6 +88,12 @@ __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int
     return make_uint4(e[0], e[1], e[2], e[3]);
 }
 
+// Whether misaligned input rows of 16-bit elements are read as aligned chunks
+// and realigned on chip (see the kernel).  4-byte elements keep the per-chunk
+// loads: four 4-byte loads per chunk already run near the copy's rate there.
+template <typename T, bool VEC_IN>
+constexpr bool kRealignInput = !VEC_IN && sizeof(T) == 2;
+
 template <typename T, int MR, int MC, int NT, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
 __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
                                                  Geometry g, bool diagonal) {
@@ -102,16 +110,41 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     constexpr int HALO = SHIFT_OUT ? V : 0;       // extra tile rows
     constexpr int HCH = HALO * MC;                // halo chunks
     constexpr int HL = SHIFT_OUT ? (HCH + NT - 1) / NT : 1;  // halo chunks per thread
-    extern __shared__ uint4 smem[];          // TR + HALO rows of MC chunks
+    // Misaligned input rows of 16-bit elements in a tile that lies wholly
+    // inside the matrix: each row segment is read as the aligned 16-byte chunks that
+    // cover it -- MC by the row's own threads, one more past its end by a
+    // helper thread -- staged as they are with a row pitch of MC + 1 chunks,
+    // and every thread then cuts its chunk's elements out of its own aligned
+    // chunk and the next one.  The extra bytes those chunks hold belong to
+    // the input's own extent (neighbouring columns, pitch padding, the row
+    // before or after) except in two tiles, which take the per-chunk path:
+    // the first tile of the first plane, whose first chunk may start before
+    // the input, and in the last plane a tile holding the last input row whose
+    // row segments end fewer than V elements before that row's end, whose last
+    // aligned chunk may reach past the input.
+    constexpr bool RAW = kRealignInput<T, VEC_IN>;
+    constexpr int XL = RAW ? (TR + NT - 1) / NT : 1;  // extra chunks per thread
+    constexpr int RP = MC + 1;                        // staging row pitch, chunks
+    extern __shared__ uint4 smem[];  // TR + HALO rows of MC chunks, or TR rows of RP
 
     pdl_prologue();
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
+    // Whether tile (b, tr, tc) takes the aligned-chunk path.
+    auto raw_tile = [&](bool full, int64_t b, int64_t tr, int64_t tc) {
+        const bool first = b == 0 && tr == 0 && tc == 0;
+        const bool last = b == g.batch - 1 && (tr + 1) * TR >= g.rows && (tc + 1) * TC + V > g.cols;
+        return RAW && full && !first && !last;
+    };
+    auto aligned_chunk = [](const T *p) {
+        return __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15)));
+    };
 
     // Phase 1a: this thread's chunks of tile `tile`, global -> registers, all
     // loads issued before any is used.
     Chunk ld[LOADS];
     Chunk hl[HL];
+    Chunk xl[XL];
     auto load_tile = [&](int64_t tile) {
         int64_t b, tr, tc;
         split_tile(g, tile, diagonal, b, tr, tc);
@@ -119,11 +152,31 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
         const int64_t r0 = tr * TR, c0 = tc * TC;
         const bool full = (r0 + TR <= g.rows) && (c0 + TC <= g.cols);
         const int64_t gc = c0 + lcc * V;
+        bool raw = false;
+        if constexpr (RAW) {
+            raw = raw_tile(full, b, tr, tc);
+            if (raw) {
+                // The aligned chunk holding this thread's first element, and
+                // for helper rows the aligned chunk past the segment (not
+                // needed when the segment ends on a 16-byte boundary, i.e.
+                // when the row is aligned).
+#pragma unroll
+                for (int k = 0; k < LOADS; ++k)
+                    ld[k].v = aligned_chunk(src + (r0 + lr + RPP * k) * g.ld_in + gc);
+#pragma unroll
+                for (int k = 0; k < XL; ++k) {
+                    const int rr = t + NT * k;
+                    if (TR % NT != 0 && rr >= TR) continue;
+                    const T *p = src + (r0 + rr) * g.ld_in + c0 + TC;
+                    if (reinterpret_cast<uintptr_t>(p) & 15u) xl[k].v = aligned_chunk(p);
+                }
+            }
+        }
         if (full && VEC_IN) {
 #pragma unroll
             for (int k = 0; k < LOADS; ++k)
                 ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + (r0 + lr + RPP * k) * g.ld_in + gc));
-        } else {
+        } else if (!raw) {
 #pragma unroll
             for (int k = 0; k < LOADS; ++k) {
                 const int64_t gr = r0 + lr + RPP * k;
@@ -211,6 +264,35 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
 
         if (!PREFETCH) load_tile(tile);
         if (tile != blockIdx.x) __syncthreads();  // previous tile fully read
+        if (RAW && raw_tile(full, b, tr, tc)) {
+            // Realign: stage the aligned chunks unshifted, then take elements
+            // s .. s+V-1 of (own chunk, next chunk), s being the row's offset
+            // from its 16-byte boundary.  Both shared passes are conflict-free
+            // (8 lanes of a phase touch 8 consecutive chunks, and the helper
+            // rows' last chunks lie RP = 1 mod 8 chunks apart).
+#pragma unroll
+            for (int k = 0; k < LOADS; ++k) smem[(lr + RPP * k) * RP + lcc] = ld[k].v;
+#pragma unroll
+            for (int k = 0; k < XL; ++k) {
+                const int rr = t + NT * k;
+                if (TR % NT != 0 && rr >= TR) continue;
+                smem[rr * RP + MC] = xl[k].v;
+            }
+            __syncthreads();
+            // Byte offsets from 16-byte boundaries: row lr's, and the step to
+            // the thread's next row (low bits of the addresses suffice).
+            const uint32_t a0 = uint32_t(reinterpret_cast<uintptr_t>(
+                in + b * g.stride_in + (r0 + lr) * g.ld_in + c0));
+            const uint32_t step = uint32_t(g.ld_in) * uint32_t(RPP * sizeof(T));
+#pragma unroll
+            for (int k = 0; k < LOADS; ++k) {
+                const int sh = int(((a0 + uint32_t(k) * step) & 15u) / sizeof(T));
+                Chunk nb;
+                nb.v = smem[(lr + RPP * k) * RP + lcc + 1];
+                ld[k].v = window<T>(ld[k], nb, sh);
+            }
+            __syncthreads();  // staging read before the tile overwrites it
+        }
         // Phase 1b: registers -> swizzled shared tile.
 #pragma unroll
         for (int k = 0; k < LOADS; ++k) {
@@ -335,7 +417,11 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
 template <typename T, int MR, int MC, int NT, bool VI, bool SO, bool PF>
 cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
-    constexpr size_t smem = size_t(V * MR + (SO ? V : 0)) * MC * 16;  // + halo rows
+    // The tile (+ halo rows), or when misaligned input rows are realigned on
+    // chip the staging rows of MC + 1 chunks, whichever is larger.
+    constexpr size_t tile_chunks = size_t(V * MR + (SO ? V : 0)) * MC;
+    constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR) * (MC + 1) : 0;
+    constexpr size_t smem = (tile_chunks > raw_chunks ? tile_chunks : raw_chunks) * 16;
     auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
     // Resident blocks per SM on each device; 0 = not set up on that device yet.
     static std::atomic<int> resident[64];

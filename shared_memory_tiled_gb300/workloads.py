@@ -25,6 +25,8 @@ The workloads follow the five configurations the library is measured on:
   from seed 4 (NaN and Inf patterns included);
 * ``c3_back``    c3's transpose back: 7919x12289 with input pitch 12289 (rows
   start at every 4-byte offset from a 16-byte boundary) and output pitch 7936.
+* ``c5_oddin``   c5 with input pitch 16385 (bf16 rows start at every 2-byte
+  offset from a 16-byte boundary), output dense.
 """
 from __future__ import annotations
 
@@ -106,6 +108,8 @@ WORKLOADS = {
     "c5": Workload("c5", "bf16", 16384, 16384, 16384, 16384, dist="bits", seed=4),
     # c3 transposed back: the odd pitch is now on the input side
     "c3_back": Workload("c3_back", "f32", 7919, 12289, 12289, 7936, dist="normal", seed=2),
+    # c5 with the odd pitch on the input side
+    "c5_oddin": Workload("c5_oddin", "bf16", 16384, 16384, 16385, 16384, dist="bits", seed=4),
 }
 
 DESCRIPTION = {
@@ -116,6 +120,7 @@ DESCRIPTION = {
     "c4": "batched fp32 [64,2048,1536] -> [64,1536,2048], uniform[-1,1) seed 3, contiguous",
     "c5": "bf16 16384x16384 (512 MiB) square, uniform random u16 bits seed 4",
     "c3_back": "fp32 7919x12289 (c3's output shape), input pitch 12289, output pitch 7936, N(0,1) seed 2",
+    "c5_oddin": "bf16 16384x16384, input pitch 16385, output dense, uniform random u16 bits seed 4",
 }
 
 

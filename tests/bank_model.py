@@ -83,6 +83,28 @@ def vec_tile_read(warp, m, V=4, MR=16, MC=16, j=0):
     return out
 
 
+def vec_tile_staging(warp, k, MC=16, next_chunk=False):
+    """Misaligned input rows: thread t's aligned chunk of load k (chunk t % MC of
+    tile row t // MC + k * 256 // MC) stored unshifted in staging rows of MC + 1
+    chunks, or with ``next_chunk`` the read of the chunk after it."""
+    out = []
+    for lane in range(32):
+        t = warp * 32 + lane
+        cc, r = t % MC, t // MC + k * (256 // MC)
+        out.append((r * (MC + 1) + cc + int(next_chunk)) * 16)
+    return out
+
+
+def vec_tile_staging_helper(warp, TR, MC=16):
+    """The helper store: thread t puts the chunk past tile row t at position MC
+    of that row's staging row (threads t >= TR hold none)."""
+    out = []
+    for lane in range(32):
+        rr = warp * 32 + lane
+        out.append((rr * (MC + 1) + MC) * 16 if rr < TR else None)
+    return out
+
+
 # --- the TMA tile with the 128-byte hardware swizzle (tile_tma.cu) ------------------------
 
 def _tma_lane(warp, lane):

@@ -77,6 +77,18 @@ def test_vector_tile_is_conflict_free(V, MR, MC):
                 assert BM.conflict_degree(BM.vec_tile_read(warp, m, V, MR, MC, j), 16) == 1
 
 
+@pytest.mark.parametrize("V,MR,MC", [(4, 16, 16), (4, 32, 16), (4, 16, 32), (4, 32, 32),
+                                     (8, 16, 16), (8, 32, 16), (8, 16, 32)])
+def test_misaligned_input_staging_is_conflict_free(V, MR, MC):
+    for warp in range(8):
+        for k in range(V * MR * MC // 256):
+            assert BM.conflict_degree(BM.vec_tile_staging(warp, k, MC), 16) == 1
+            assert BM.conflict_degree(BM.vec_tile_staging(warp, k, MC, next_chunk=True), 16) == 1
+        a = BM.vec_tile_staging_helper(warp, V * MR, MC)
+        if any(x is not None for x in a):
+            assert BM.conflict_degree(a, 16) == 1
+
+
 def test_vector_tile_without_swizzle_would_conflict():
     # the same micro-block read on a plain row-major tile: 8 lanes, one chunk column
     plain = [((4 * lane + 0) * 16 + 0) * 16 for lane in range(32)]

@@ -71,6 +71,13 @@ def test_shifted_store_tile_budget(vec_report):
     assert k["regs"] <= 88 and k["spill"] == 0
 
 
+def test_realigned_input_tile_budget(vec_report):
+    # bf16 128x128 with misaligned input rows (aligned chunks realigned on
+    # chip): 80 registers keep 3 blocks of 256 threads per SM
+    k = _find(vec_report, "k_tile_vecItLi16ELi16ELi256ELb0ELb0ELb0E")
+    assert k["regs"] <= 80 and k["spill"] == 0
+
+
 def test_inplace_budgets():
     # fp32: both tiles' loads in flight, 4 blocks/SM; bf16: staged one tile
     # after the other, 3 blocks/SM (64 KiB of shared memory each)

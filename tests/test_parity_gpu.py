@@ -123,6 +123,27 @@ def test_misaligned_base_pointers(dtype):
 
 
 @pytest.mark.parametrize("dtype", [U32, U16], ids=["f32", "bf16"])
+def test_input_pitch_not_a_multiple_of_16_bytes(dtype):
+    """Odd input pitches and base offsets.  bf16 tiles inside the matrix read
+    aligned 16-byte chunks and realign them on chip, except the first tile and
+    a tile holding the last row whose segments end within one chunk of its end
+    (per-chunk loads there); the shapes put full tiles against both of those
+    edges, with one or more planes and aligned or odd output pitches."""
+    vec = 16 // np.dtype(dtype).itemsize
+    kws = [dict(variant=V.AUTO), dict(variant=V.TILE_VEC, schedule=2)] + \
+        [dict(variant=V.TILE_VEC, tile_rows=r, tile_cols=c) for r, c in VEC_SHAPES[dtype]] + \
+        [dict(variant=V.TILE_VEC, threads=128, tile_rows=r, tile_cols=c) for r, c in VEC_128[dtype]]
+    for (b, r, c, pi, po, pp) in [(1, 256, 256, 1, 0, 0), (1, 256, 257, 3, 0, 0),
+                                  (2, 256, 256 + vec - 1, 5, 0, 3), (1, 256, 256 + vec, 1, 0, 0),
+                                  (1, 384, 264, 1, 1, 0), (3, 129, 385, 7, 3, 2),
+                                  (2, 512, 128, 2, 5, 0)]:
+        x, prefill, geo = case(dtype, b, r, c, pi, po, pp, seed=r + c + pi)
+        for in_off in (0, 1, vec - 1):
+            for kw in kws:
+                check(x, prefill, geo, in_off=in_off, **kw)
+
+
+@pytest.mark.parametrize("dtype", [U32, U16], ids=["f32", "bf16"])
 def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
     """Odd output pitches: every output row starts at a different offset from a
     16-byte boundary (the shifted-store path), full tiles and ragged edges."""
