@@ -272,21 +272,26 @@ def transpose(x, out=None, *, variant=Variant.AUTO, pad=0, ctas_per_sm=0, stages
                      stream)
     opts = make_options(variant, pad, ctas_per_sm, stages, tile_order, out_stages, tile_rows,
                         tile_cols, schedule, threads)
-    check(tr_transpose_ex(args, opts))
+    with torch.cuda.device(x.device):  # the library sets kernels up per current device
+        check(tr_transpose_ex(args, opts))
     return out
 
 
 def copy(src, dst, stream=None):
-    """Byte copy of a contiguous CUDA tensor into another of the same byte size."""
+    """Byte copy of a contiguous CUDA tensor into another of the same byte size
+    (on the same device)."""
     import torch
     if not (src.is_cuda and dst.is_cuda and src.is_contiguous() and dst.is_contiguous()):
         raise ValueError("copy wants contiguous CUDA tensors")
     n = src.numel() * src.element_size()
     if n != dst.numel() * dst.element_size():
         raise ValueError("size mismatch")
+    if src.device != dst.device:
+        raise ValueError("copy wants both tensors on one device")
     if stream is None:
         stream = torch.cuda.current_stream(src.device).cuda_stream
-    check(tr_copy(src.data_ptr(), dst.data_ptr(), n, stream))
+    with torch.cuda.device(src.device):
+        check(tr_copy(src.data_ptr(), dst.data_ptr(), n, stream))
     return dst
 
 
@@ -302,5 +307,6 @@ def transpose_(x, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     f = tr_transpose_inplace_f32 if dt == DType.F32 else tr_transpose_inplace_bf16
-    check(f(x.data_ptr(), b, r, ld, s, stream))
+    with torch.cuda.device(x.device):
+        check(f(x.data_ptr(), b, r, ld, s, stream))
     return x
