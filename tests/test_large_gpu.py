@@ -84,7 +84,7 @@ def test_inplace_beyond_2_31_elements():
                          ids=["odd-output-pitch", "odd-input-pitch"])
 def test_fp32_misaligned_pitches_beyond_2_31_elements(ld_in, ld_out):
     """Past 2**31 elements with rows that start off 16-byte boundaries: the
-    shifted stores (with their halo rows) on the output side, single-element
+    shifted stores (with their halo rows) on the output side, per-chunk 4-byte
     loads on the input side."""
     import torch
     rows, cols = 65537, 32801          # 2,149,679,137 elements
@@ -95,6 +95,29 @@ def test_fp32_misaligned_pitches_beyond_2_31_elements(ld_in, ld_out):
     torch.cuda.synchronize()
     _sampled_check(x, out, rows, cols, ld_in, ld_out, seed=3)
     # every output row ends where it should: the element after it (pitch padding) is untouched
+    pad = out.view(cols, ld_out)[:, rows:]
+    assert int(torch.count_nonzero(pad)) == 0
+    xs = x.view(rows, ld_in)[:, :cols].to(torch.int64).sum()
+    os_ = out.view(cols, ld_out)[:, :rows].to(torch.int64).sum()
+    assert int(xs) == int(os_)
+    del x, out, pad
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("ld_in,ld_out", [(32803, 65544), (32803, 65539)],
+                         ids=["odd-input-pitch", "both-pitches-odd"])
+def test_bf16_misaligned_pitches_beyond_2_31_elements(ld_in, ld_out):
+    """bf16 past 2**31 elements with input rows at every 2-byte offset from a
+    16-byte boundary: aligned chunks realigned on chip (row offsets taken from
+    the low 32 bits of the addresses), alone and with shifted stores."""
+    import torch
+    rows, cols = 65537, 32801          # 2,149,679,137 elements, 4.3 GB each way
+    x = torch.randint(-2**15, 2**15 - 1, (rows * ld_in,), dtype=torch.int16, device="cuda")
+    out = torch.zeros(cols * ld_out, dtype=torch.int16, device="cuda")
+    args = B.make_args(x.data_ptr(), out.data_ptr(), B.DType.BF16, 1, rows, cols, ld_in, ld_out)
+    B.check(B.tr_transpose_ex(args, B.make_options(B.Variant.AUTO)))
+    torch.cuda.synchronize()
+    _sampled_check(x, out, rows, cols, ld_in, ld_out, seed=5)
     pad = out.view(cols, ld_out)[:, rows:]
     assert int(torch.count_nonzero(pad)) == 0
     xs = x.view(rows, ld_in)[:, :cols].to(torch.int64).sum()
