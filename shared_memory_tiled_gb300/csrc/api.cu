@@ -126,7 +126,8 @@ int32_t choose(const Problem &p, const tr_options *o) {
 // chunks realigned on chip) takes 64x128 tiles on 128 threads: 16384x16384
 // bf16 with input pitch 16385 reaches 6598 GB/s, against 5961 with 128x128 on
 // 256 threads, 5848 with 128x128 on 128 and 5566 with 256x64 on 256; with the
-// output pitch odd as well, 4363 against 3661 with 128x128 on 256.  Otherwise
+// output pitch odd as well, 4363 against 3661 with 128x128 on 256 (4576 since
+// the halo rows are realigned too).  Otherwise
 // output rows that are not 16-byte aligned (shifted stores) take 128-row tiles,
 // 16 chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s
 // with 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16

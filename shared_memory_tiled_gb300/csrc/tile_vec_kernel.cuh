@@ -111,30 +111,31 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     constexpr int HCH = HALO * MC;                // halo chunks
     constexpr int HL = SHIFT_OUT ? (HCH + NT - 1) / NT : 1;  // halo chunks per thread
     // Misaligned input rows of 16-bit elements in a tile that lies wholly
-    // inside the matrix: each row segment is read as the aligned 16-byte chunks that
-    // cover it -- MC by the row's own threads, one more past its end by a
-    // helper thread -- staged as they are with a row pitch of MC + 1 chunks,
-    // and every thread then cuts its chunk's elements out of its own aligned
-    // chunk and the next one.  The extra bytes those chunks hold belong to
-    // the input's own extent (neighbouring columns, pitch padding, the row
-    // before or after) except in two tiles, which take the per-chunk path:
-    // the first tile of the first plane, whose first chunk may start before
-    // the input, and in the last plane a tile holding the last input row whose
-    // row segments end fewer than V elements before that row's end, whose last
-    // aligned chunk may reach past the input.
+    // inside the matrix, halo rows included: each row segment is read as the
+    // aligned 16-byte chunks that cover it -- MC by the row's own threads, one
+    // more past its end by a helper thread -- staged as they are with a row
+    // pitch of MC + 1 chunks, and every thread then cuts its chunk's elements
+    // out of its own aligned chunk and the next one.  The extra bytes those
+    // chunks hold belong to the input's own extent (neighbouring columns,
+    // pitch padding, the row before or after) except in two tiles, which take
+    // the per-chunk path: the first tile of the first plane, whose first chunk
+    // may start before the input, and in the last plane a tile reading the
+    // last input row whose row segments end fewer than V elements before that
+    // row's end, whose last aligned chunk may reach past the input.
     constexpr bool RAW = kRealignInput<T, VEC_IN>;
-    constexpr int XL = RAW ? (TR + NT - 1) / NT : 1;  // extra chunks per thread
-    constexpr int RP = MC + 1;                        // staging row pitch, chunks
-    extern __shared__ uint4 smem[];  // TR + HALO rows of MC chunks, or TR rows of RP
+    constexpr int XL = RAW ? (TR + HALO + NT - 1) / NT : 1;  // extra chunks per thread
+    constexpr int RP = MC + 1;                               // staging row pitch, chunks
+    extern __shared__ uint4 smem[];  // TR + HALO rows of MC chunks, or of RP
 
     pdl_prologue();
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
     // Whether tile (b, tr, tc) takes the aligned-chunk path.
     auto raw_tile = [&](bool full, int64_t b, int64_t tr, int64_t tc) {
+        const int64_t end = (tr + 1) * TR + HALO;  // one past the last row read
         const bool first = b == 0 && tr == 0 && tc == 0;
-        const bool last = b == g.batch - 1 && (tr + 1) * TR >= g.rows && (tc + 1) * TC + V > g.cols;
-        return RAW && full && !first && !last;
+        const bool last = b == g.batch - 1 && end >= g.rows && (tc + 1) * TC + V > g.cols;
+        return RAW && full && end <= g.rows && !first && !last;
     };
     auto aligned_chunk = [](const T *p) {
         return __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15)));
@@ -157,16 +158,16 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
             raw = raw_tile(full, b, tr, tc);
             if (raw) {
                 // The aligned chunk holding this thread's first element, and
-                // for helper rows the aligned chunk past the segment (not
-                // needed when the segment ends on a 16-byte boundary, i.e.
-                // when the row is aligned).
+                // for helper rows (tile and halo rows) the aligned chunk past
+                // the segment (not needed when the segment ends on a 16-byte
+                // boundary, i.e. when the row is aligned).
 #pragma unroll
                 for (int k = 0; k < LOADS; ++k)
                     ld[k].v = aligned_chunk(src + (r0 + lr + RPP * k) * g.ld_in + gc);
 #pragma unroll
                 for (int k = 0; k < XL; ++k) {
                     const int rr = t + NT * k;
-                    if (TR % NT != 0 && rr >= TR) continue;
+                    if ((TR + HALO) % NT != 0 && rr >= TR + HALO) continue;
                     const T *p = src + (r0 + rr) * g.ld_in + c0 + TC;
                     if (reinterpret_cast<uintptr_t>(p) & 15u) xl[k].v = aligned_chunk(p);
                 }
@@ -227,7 +228,9 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                 if (HCH % NT != 0 && h >= HCH) continue;
                 const int64_t gr = r0 + TR + h / MC;
                 const int64_t hc = c0 + (h % MC) * V;
-                if (VEC_IN && gr < g.rows && hc + V <= g.cols) {
+                if (raw) {
+                    hl[k].v = aligned_chunk(src + gr * g.ld_in + hc);
+                } else if (VEC_IN && gr < g.rows && hc + V <= g.cols) {
                     hl[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + hc));
                 } else {
                     T e[V];
@@ -272,10 +275,18 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
             // rows' last chunks lie RP = 1 mod 8 chunks apart).
 #pragma unroll
             for (int k = 0; k < LOADS; ++k) smem[(lr + RPP * k) * RP + lcc] = ld[k].v;
+            if constexpr (SHIFT_OUT) {
+#pragma unroll
+                for (int k = 0; k < HL; ++k) {
+                    const int h = t + NT * k;
+                    if (HCH % NT != 0 && h >= HCH) continue;
+                    smem[(TR + h / MC) * RP + h % MC] = hl[k].v;
+                }
+            }
 #pragma unroll
             for (int k = 0; k < XL; ++k) {
                 const int rr = t + NT * k;
-                if (TR % NT != 0 && rr >= TR) continue;
+                if ((TR + HALO) % NT != 0 && rr >= TR + HALO) continue;
                 smem[rr * RP + MC] = xl[k].v;
             }
             __syncthreads();
@@ -290,6 +301,21 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                 Chunk nb;
                 nb.v = smem[(lr + RPP * k) * RP + lcc + 1];
                 ld[k].v = window<T>(ld[k], nb, sh);
+            }
+            if constexpr (SHIFT_OUT) {
+#pragma unroll
+                for (int k = 0; k < HL; ++k) {
+                    const int h = t + NT * k;
+                    if (HCH % NT != 0 && h >= HCH) continue;
+                    const int r = TR + h / MC;
+                    const int sh = int((reinterpret_cast<uintptr_t>(
+                                            in + b * g.stride_in + (r0 + r) * g.ld_in + c0) &
+                                        15u) /
+                                       sizeof(T));
+                    Chunk nb;
+                    nb.v = smem[r * RP + h % MC + 1];
+                    hl[k].v = window<T>(hl[k], nb, sh);
+                }
             }
             __syncthreads();  // staging read before the tile overwrites it
         }
@@ -420,7 +446,7 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
     // The tile (+ halo rows), or when misaligned input rows are realigned on
     // chip the staging rows of MC + 1 chunks, whichever is larger.
     constexpr size_t tile_chunks = size_t(V * MR + (SO ? V : 0)) * MC;
-    constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR) * (MC + 1) : 0;
+    constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR + (SO ? V : 0)) * (MC + 1) : 0;
     constexpr size_t smem = (tile_chunks > raw_chunks ? tile_chunks : raw_chunks) * 16;
     auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
     // Resident blocks per SM on each device; 0 = not set up on that device yet.

@@ -2,14 +2,14 @@
 (tile_vec_kernel.cuh).
 
 When input rows do not start on 16-byte boundaries, a tile that lies wholly
-inside the matrix reads each of its row segments as the aligned 16-byte chunks
-that cover it: thread lcc the chunk holding its first element, and a helper
+inside the matrix (with shifted stores, its halo rows below included) reads
+each of its row segments as the aligned 16-byte chunks that cover it: thread lcc the chunk holding its first element, and a helper
 thread the chunk past the segment's end when the row is not aligned.  Every
 thread then takes elements s .. s+V-1 of (its chunk, the next chunk), s being
 the row's element offset from its 16-byte boundary, which the kernel derives
 from the low 32 bits of one row address and a per-row step.  Two tiles take the
 per-chunk path instead: the first tile of the first plane, and a tile in the
-last plane holding the last input row whose row segments end fewer than V
+last plane reading the last input row whose row segments end fewer than V
 elements before that row's end.
 
 The model restates those rules and checks, over a sweep of shapes, pitches,
@@ -28,13 +28,14 @@ import pytest
 M32 = (1 << 32) - 1
 
 
-def _raw_tile(g, TR, TC, V, full, b, tr, tc):
+def _raw_tile(g, TR, TC, V, full, b, tr, tc, halo=0):
+    end = (tr + 1) * TR + halo  # one past the last row the tile reads
     first = b == 0 and tr == 0 and tc == 0
-    last = b == g["batch"] - 1 and (tr + 1) * TR >= g["rows"] and (tc + 1) * TC + V > g["cols"]
-    return full and not first and not last
+    last = b == g["batch"] - 1 and end >= g["rows"] and (tc + 1) * TC + V > g["cols"]
+    return full and end <= g["rows"] and not first and not last
 
 
-def _check(esize, TR, TC, RPP, batch, rows, cols, ld_in, gap, base_elems):
+def _check(esize, TR, TC, RPP, batch, rows, cols, ld_in, gap, base_elems, halo):
     V = 16 // esize
     MC = TC // V
     stride = (rows - 1) * ld_in + cols + gap if batch > 1 else rows * ld_in
@@ -51,35 +52,36 @@ def _check(esize, TR, TC, RPP, batch, rows, cols, ld_in, gap, base_elems):
     for b, tr, tc in itertools.product(range(batch), range(tiles_r), range(tiles_c)):
         r0, c0 = tr * TR, tc * TC
         full = r0 + TR <= rows and c0 + TC <= cols
-        if not _raw_tile(g, TR, TC, V, full, b, tr, tc):
+        if not _raw_tile(g, TR, TC, V, full, b, tr, tc, halo):
             continue
         raw_tiles += 1
-        for lr in range(RPP):  # the rows one thread visits: lr, lr + RPP, ...
-            a_first = (lead + b * stride + (r0 + lr) * ld_in + c0) * esize
-            a0 = a_first & M32
+        for lr in range(RPP):  # the tile rows one thread visits: lr, lr + RPP, ...
+            a0 = ((lead + b * stride + (r0 + lr) * ld_in + c0) * esize) & M32
             step = (ld_in * RPP * esize) & M32
             for k in range(TR // RPP):
-                r = lr + RPP * k
-                a_row = (lead + b * stride + (r0 + r) * ld_in + c0) * esize
-                sh = (((a0 + k * step) & M32) & 15) // esize
-                assert sh == (a_row & 15) // esize                                  # (3)
-                chunks = [((a_row + 16 * c) & ~15) for c in range(MC)]
-                if a_row & 15:
-                    chunks.append((a_row + 16 * MC) & ~15)                          # helper's
-                for a in chunks:
-                    assert in_lo <= a and a + 16 <= in_hi, (b, tr, tc, r, a - in_lo)  # (1)
-                for c in range(MC):
-                    own = arena[chunks[c] // esize: chunks[c] // esize + V]
-                    nxt = (arena[chunks[c + 1] // esize: chunks[c + 1] // esize + V]
-                           if c + 1 < len(chunks) else np.zeros(V, np.int64))
-                    got = np.concatenate([own, nxt])[sh: sh + V]
-                    first = b * stride + (r0 + r) * ld_in + c0 + c * V
-                    assert np.array_equal(got, np.arange(first, first + V)), (b, tr, tc, r, c)  # (2)
+                a_row = (lead + b * stride + (r0 + lr + RPP * k) * ld_in + c0) * esize
+                assert (((a0 + k * step) & M32) & 15) == a_row & 15                 # (3)
+        for r in range(TR + halo):  # tile rows, then halo rows
+            a_row = (lead + b * stride + (r0 + r) * ld_in + c0) * esize
+            sh = (a_row & 15) // esize
+            chunks = [((a_row + 16 * c) & ~15) for c in range(MC)]
+            if a_row & 15:
+                chunks.append((a_row + 16 * MC) & ~15)                          # helper's
+            for a in chunks:
+                assert in_lo <= a and a + 16 <= in_hi, (b, tr, tc, r, a - in_lo)  # (1)
+            for c in range(MC):
+                own = arena[chunks[c] // esize: chunks[c] // esize + V]
+                nxt = (arena[chunks[c + 1] // esize: chunks[c + 1] // esize + V]
+                       if c + 1 < len(chunks) else np.zeros(V, np.int64))
+                got = np.concatenate([own, nxt])[sh: sh + V]
+                first = b * stride + (r0 + r) * ld_in + c0 + c * V
+                assert np.array_equal(got, np.arange(first, first + V)), (b, tr, tc, r, c)  # (2)
     return raw_tiles
 
 
+@pytest.mark.parametrize("halo", [False, True], ids=["aligned-output", "shifted-stores"])
 @pytest.mark.parametrize("esize", [4, 2])
-def test_aligned_chunk_loads_stay_inside_the_input(esize):
+def test_aligned_chunk_loads_stay_inside_the_input(esize, halo):
     V = 16 // esize
     total_raw = 0
     for TR, TC, RPP in [(8 * V, 8 * V, 4), (16 * V, 8 * V, 8), (8 * V, 16 * V, 16)]:
@@ -89,7 +91,7 @@ def test_aligned_chunk_loads_stay_inside_the_input(esize):
                     for batch, gap in ((1, 0), (2, 0), (3, 5)):
                         for base in range(V):
                             total_raw += _check(esize, TR, TC, RPP, batch, rows, cols, ld_in, gap,
-                                                base)
+                                                base, V if halo else 0)
     assert total_raw > 0
 
 
