@@ -131,7 +131,8 @@ int32_t choose(const Problem &p, const tr_options *o) {
 // output rows that are not 16-byte aligned (shifted stores) take 128-row tiles,
 // 16 chunks wide: 12289x7919 fp32 with output pitch 12289 reaches 6668 GB/s
 // with 128x64 against 5849 with 64x64 and 5843 with 128x128; 16384x16384 bf16
-// with output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128.  A
+// with output pitch 16385 5630 GB/s with 128x128 against 5070 with 256x128,
+// 5612 with 64x128 on 128 threads and 5388 with 128x128 on 128.  A
 // misaligned fp32 input takes tiles 16 chunks tall and 128 elements wide:
 // 7919x12289 fp32 with input pitch 12289 reaches 6751 GB/s with 64x128
 // against 5999 with 64x64 and 5952 / 6171 with 128x64 / 64x64 on 128 threads.
