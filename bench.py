@@ -162,6 +162,34 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def nvsmi_id(local_rank):
+    """The id nvidia-smi knows CUDA device ``local_rank`` by: its UUID when
+    torch reports one and nvidia-smi accepts it, else the entry of
+    CUDA_VISIBLE_DEVICES, else the ordinal (CUDA ordinals and nvidia-smi
+    indices differ once CUDA_VISIBLE_DEVICES remaps the devices)."""
+    candidates = []
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        if u:
+            candidates.append(u if u.startswith("GPU-") else "GPU-" + u)
+    except Exception:
+        pass
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if local_rank < len(vis):
+        candidates.append(vis[local_rank])
+    for c in candidates:
+        try:
+            r = subprocess.run(["nvidia-smi", f"--id={c}", "--query-gpu=index",
+                                "--format=csv,noheader"], capture_output=True, text=True,
+                               timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                return c
+        except Exception:
+            break
+    return str(local_rank)
+
+
 def host_cpu_model():
     """The host CPU's model name, as lscpu or /proc/cpuinfo report it."""
     try:
@@ -382,7 +410,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return [evs[i].elapsed_time(evs[i + 1]) for i in range(k)]
 
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(nvsmi_id(local_rank))
     sampler.start()
     # ---- the timed region: exactly K transposes
     t_wall0 = time.time()

@@ -75,3 +75,20 @@ def test_recorded_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
     else:
         assert rec == (None, None)
     assert bench.recorded_traffic("k_tile_vec", "no_such_workload") == (None, None)
+
+
+def test_clock_samples_follow_the_visible_device(monkeypatch):
+    """With CUDA_VISIBLE_DEVICES remapping devices, the clock sampler asks
+    nvidia-smi for the GPU the process runs on, not the one with its ordinal."""
+    import bench
+
+    def fake_run(cmd, **kw):
+        ok = cmd[:2] == ["nvidia-smi", "--id=5"]
+        return subprocess.CompletedProcess(cmd, 0 if ok else 6, stdout="5\n" if ok else "",
+                                           stderr="")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3,5")
+    assert bench.nvsmi_id(1) == "5"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "")
+    assert bench.nvsmi_id(1) == "1"
