@@ -260,6 +260,27 @@ tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *
  * tr_status on invalid arguments.  Makes no CUDA call. */
 int32_t tr_plan_variant(const tr_args *args, const tr_options *opts);
 
+/* What tr_transpose_ex would launch, as tr_plan_ex reports it. */
+typedef struct tr_plan {
+    int32_t variant;    /* tr_variant, never AUTO                                          */
+    int32_t tile_rows;  /* TILE_VEC: tile rows in elements (0 for the other variants)       */
+    int32_t tile_cols;  /* TILE_VEC: tile columns in elements                               */
+    int32_t threads;    /* TILE_VEC: threads per block                                     */
+    int32_t schedule;   /* TILE_VEC: 0 one tile per block, 2 persistent with prefetch       */
+    int32_t vec_in;     /* 1 when input rows, base and plane pitch sit on 16-byte boundaries */
+    int32_t vec_out;    /* the same for the output (else TILE_VEC shifts its stores)        */
+} tr_plan;
+
+/* Host-only planning in full: fills *plan with the variant and, for the
+ * vector tile, the tile shape and block size that AUTO or the options
+ * request (see tr_options), and which sides allow 16-byte accesses.  Returns
+ * TR_OK, TR_ERR_NULL for a NULL plan, or the argument error tr_transpose_ex
+ * would return (TR_ERR_UNSUPPORTED for TMA on a misaligned side or a TMA
+ * schedule on the vector tile).  A tile shape and block size that the vector
+ * tile does not have (see tr_options) are reported as requested and refused
+ * by tr_transpose_ex.  Makes no CUDA call. */
+tr_status tr_plan_ex(const tr_args *args, const tr_options *opts, tr_plan *plan);
+
 /* Reads and clears the device-side fault flag of the CURRENT device after
  * synchronizing it: TR_ERR_TIMEOUT if a bounded in-kernel wait ran out since
  * the last call, TR_OK otherwise (TR_ERR_CUDA if the read itself fails). */

@@ -69,6 +69,13 @@ class Args(ctypes.Structure):
                 ("stride_in", I64), ("stride_out", I64), ("stream", VP)]
 
 
+class Plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
+                ("tile_cols", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("schedule", ctypes.c_int32), ("vec_in", ctypes.c_int32),
+                ("vec_out", ctypes.c_int32)]
+
+
 class LibraryMissing(RuntimeError):
     pass
 
@@ -90,6 +97,8 @@ SIGNATURES = {
     "tr_transpose_inplace_f32": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_transpose_inplace_bf16": ([VP, I64, I64, I64, I64, VP], ctypes.c_int),
     "tr_plan_variant": ([ctypes.POINTER(Args), ctypes.POINTER(Options)], ctypes.c_int32),
+    "tr_plan_ex": ([ctypes.POINTER(Args), ctypes.POINTER(Options), ctypes.POINTER(Plan)],
+                   ctypes.c_int),
     "tr_bank_probe": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, VP, VP], ctypes.c_int),
     "tr_operand_tiles_f32": ([VP, VP, I64, I64, I64, ctypes.c_int32, ctypes.c_int32,
                               ctypes.c_int32, VP], ctypes.c_int),
@@ -179,6 +188,11 @@ def tr_copy(in_ptr, out_ptr, nbytes, stream=0) -> int:
 
 def tr_plan_variant(args: Args, opts: Options | None = None) -> int:
     return _call("tr_plan_variant", ctypes.byref(args), ctypes.byref(opts) if opts else None)
+
+
+def tr_plan_ex(args: Args, opts: Options | None, plan: Plan) -> int:
+    return _call("tr_plan_ex", ctypes.byref(args), ctypes.byref(opts) if opts else None,
+                 ctypes.byref(plan) if plan is not None else None)
 
 
 def tr_operand_tiles_f32(a_ptr, out_ptr, m, k, lda, bm, bk, pad=-1, stream=0) -> int:

@@ -153,6 +153,16 @@ void auto_vec_shape(const Problem &p, bool in16, bool out16, VecConfig *cfg) {
     }
 }
 
+// The vector tile's configuration for these options: the caller's tile
+// shape, block size, tile order and schedule, with AUTO's shape and block
+// size (auto_vec_shape) where no tile shape is given.
+VecConfig vec_config(const Problem &p, const tr_options *o, bool in16, bool out16) {
+    VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
+                  o && o->schedule == 2, o ? o->threads : 0};
+    if (cfg.tile_rows == 0 && cfg.tile_cols == 0) auto_vec_shape(p, in16, out16, &cfg);
+    return cfg;
+}
+
 tr_status run(const tr_args *a, const tr_options *o) {
     Problem p{};
     bool empty = false;
@@ -173,9 +183,7 @@ tr_status run(const tr_args *a, const tr_options *o) {
                           cudaSuccess);
                 return TR_ERR_UNSUPPORTED;
             }
-            VecConfig cfg{o ? o->tile_order : 0, o ? o->tile_rows : 0, o ? o->tile_cols : 0,
-                          o && o->schedule == 2, o ? o->threads : 0};
-            if (cfg.tile_rows == 0 && cfg.tile_cols == 0) auto_vec_shape(p, in16, out16, &cfg);
+            const VecConfig cfg = vec_config(p, o, in16, out16);
             const char *why = nullptr;
             e = launch_tile_vec(p, in16, out16, cfg, &why);
             if (e != cudaSuccess && why) {
@@ -369,6 +377,38 @@ tr_status tr_bank_probe(int32_t layout, int32_t reps, int32_t blocks, uint32_t *
     if (e != cudaSuccess) {
         tr::set_error("bank probe launch failed", e);
         return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
+tr_status tr_plan_ex(const tr_args *args, const tr_options *opts, tr_plan *plan) {
+    if (!plan) return TR_ERR_NULL;
+    *plan = tr_plan{};
+    tr::Problem p{};
+    bool empty = false;
+    if (!tr::options_valid(opts)) return TR_ERR_UNSUPPORTED;
+    const tr_status st = tr::validate(args, &p, &empty);
+    if (st != TR_OK) return st;
+    if (empty) {
+        p = tr::Problem{args->in, args->out, args->dtype == TR_DTYPE_F32 ? 4 : 2, args->batch,
+                        args->rows, args->cols, args->ld_in, args->ld_out, args->stride_in,
+                        args->stride_out, nullptr};
+    }
+    plan->variant = tr::choose(p, opts);
+    const bool in16 = tr::side_aligned16(p.in, p.ld_in, p.stride_in, p.batch, p.esize);
+    const bool out16 = tr::side_aligned16(p.out, p.ld_out, p.stride_out, p.batch, p.esize);
+    plan->vec_in = in16;
+    plan->vec_out = out16;
+    if (plan->variant == TR_VARIANT_TILE_VEC) {
+        if (opts && opts->schedule >= 3) return TR_ERR_UNSUPPORTED;
+        const tr::VecConfig cfg = tr::vec_config(p, opts, in16, out16);
+        const int v = 16 / p.esize;  // 16 x 16 chunks when a dimension is left to the kernel
+        plan->tile_rows = cfg.tile_rows ? cfg.tile_rows : 16 * v;
+        plan->tile_cols = cfg.tile_cols ? cfg.tile_cols : 16 * v;
+        plan->threads = cfg.threads ? cfg.threads : 256;
+        plan->schedule = cfg.prefetch ? 2 : 0;
+    } else if (plan->variant == TR_VARIANT_TMA && !(in16 && out16)) {
+        return TR_ERR_UNSUPPORTED;
     }
     return TR_OK;
 }

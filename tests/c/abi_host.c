@@ -42,6 +42,19 @@ int main(void) {
     a.ld_in = 8192;
     a.ld_out = 8192;
     expect(tr_plan_variant(&a, NULL) == TR_VARIANT_TILE_VEC, "AUTO plans the vector tile");
+    {
+        tr_plan plan;
+        expect(tr_plan_ex(&a, NULL, &plan) == TR_OK && plan.variant == TR_VARIANT_TILE_VEC &&
+                   plan.tile_rows == 64 && plan.tile_cols == 64 && plan.threads == 256 &&
+                   plan.vec_in == 1 && plan.vec_out == 1,
+               "AUTO's tile for the aligned 8192 x 8192 fp32 case");
+        a.ld_out = 8193;
+        expect(tr_plan_ex(&a, NULL, &plan) == TR_OK && plan.tile_rows == 128 &&
+                   plan.tile_cols == 64 && plan.vec_out == 0,
+               "AUTO's tile for an odd output pitch");
+        a.ld_out = 8192;
+        expect(tr_plan_ex(&a, NULL, NULL) == TR_ERR_NULL, "NULL plan");
+    }
     o.variant = TR_VARIANT_TMA;
     expect(tr_plan_variant(&a, &o) == TR_VARIANT_TMA, "explicit TMA honoured");
     o.stages = 1;

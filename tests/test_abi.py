@@ -146,6 +146,66 @@ def test_planner(lib):
     assert _plan(FAKE_IN, FAKE_OUT, 7, 1, 4, 4, 4, 4) == -B.Status.ERR_UNSUPPORTED
 
 
+def _plan_ex(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, si=0, so=0, **opt):
+    a = B.make_args(in_ptr, out_ptr, dtype, batch, rows, cols, ld_in, ld_out, si, so)
+    p = B.Plan()
+    st = B.tr_plan_ex(a, B.make_options(**opt) if opt else None, p)
+    return st, p
+
+
+def test_plan_ex_reports_the_tile_auto_takes(lib):
+    """AUTO's vector-tile shape and block size for each alignment class, as the
+    header documents them (tile rows, tile cols, threads, vec_in, vec_out)."""
+    F32, BF16 = B.DType.F32, B.DType.BF16
+    cases = [
+        ((F32, 1, 8192, 8192, 8192, 8192), (64, 64, 256, 1, 1)),                  # C2
+        ((F32, 1, 12289, 7919, 7936, 12289), (128, 64, 256, 1, 0)),              # C3
+        ((F32, 64, 2048, 1536, 1536, 2048, 2048 * 1536, 1536 * 2048), (64, 64, 256, 1, 1)),
+        ((BF16, 1, 16384, 16384, 16384, 16384), (128, 128, 256, 1, 1)),          # C5
+        ((F32, 1, 7919, 12289, 12289, 7936), (64, 128, 256, 0, 1)),              # C3 back
+        ((BF16, 1, 16384, 16384, 16385, 16384), (64, 128, 128, 0, 1)),           # odd input
+        ((BF16, 1, 16384, 16384, 16385, 16385), (64, 128, 128, 0, 0)),           # both odd
+        ((BF16, 1, 16384, 16384, 16384, 16385), (128, 128, 256, 1, 0)),          # odd output
+        ((F32, 2, 64, 64, 64, 64, 64 * 64 + 1, 64 * 64), (64, 128, 256, 0, 1)),  # plane pitch
+    ]
+    for args, want in cases:
+        st, p = _plan_ex(FAKE_IN, FAKE_OUT, *args)
+        assert st == B.Status.OK and p.variant == B.Variant.TILE_VEC, args
+        assert (p.tile_rows, p.tile_cols, p.threads, p.vec_in, p.vec_out) == want, args
+        assert p.schedule == 0
+    st, p = _plan_ex(FAKE_IN + 4, FAKE_OUT, F32, 1, 64, 64, 64, 64)              # base pointer
+    assert (p.tile_rows, p.tile_cols, p.threads, p.vec_in, p.vec_out) == (64, 128, 256, 0, 1)
+
+
+def test_plan_ex_reports_requests_and_refusals(lib):
+    F32, BF16, V = B.DType.F32, B.DType.BF16, B.Variant
+    # a block size set by the caller keeps bf16's 128x128 tile for a misaligned input
+    st, p = _plan_ex(FAKE_IN, FAKE_OUT, BF16, 1, 4096, 4096, 4097, 4096, variant=V.TILE_VEC,
+                     threads=256)
+    assert (st, p.tile_rows, p.tile_cols, p.threads) == (B.Status.OK, 128, 128, 256)
+    # explicit shapes and the prefetching schedule are reported as requested
+    st, p = _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 64, 64, variant=V.TILE_VEC,
+                     tile_rows=128, tile_cols=32, schedule=2)
+    assert (st, p.tile_rows, p.tile_cols, p.threads, p.schedule) == (B.Status.OK, 128, 32, 256, 2)
+    st, p = _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 64, 64, variant=V.TILE_VEC, tile_rows=128)
+    assert (p.tile_rows, p.tile_cols) == (128, 64)
+    # the other variants carry no tile shape
+    for v in (V.TMA, V.TILE_PAD, V.NAIVE_ROW, V.NAIVE_COL):
+        st, p = _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 64, 64, variant=v)
+        assert st == B.Status.OK and p.variant == v and (p.tile_rows, p.threads) == (0, 0)
+        assert (p.vec_in, p.vec_out) == (1, 1)
+    # refusals match tr_transpose_ex's argument checks
+    assert _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 65, 64, variant=V.TMA)[0] == \
+        B.Status.ERR_UNSUPPORTED
+    assert _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 64, 64, 64, 64, variant=V.TILE_VEC,
+                    schedule=3)[0] == B.Status.ERR_UNSUPPORTED
+    assert _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 4, 5, 4, 4)[0] == B.Status.ERR_BAD_LD
+    assert _plan_ex(FAKE_IN + 2, FAKE_OUT, F32, 1, 4, 4, 4, 4)[0] == B.Status.ERR_UNSUPPORTED
+    assert _plan_ex(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4, pad=5)[0] == B.Status.ERR_UNSUPPORTED
+    a = B.make_args(FAKE_IN, FAKE_OUT, F32, 1, 4, 4, 4, 4)
+    assert B.tr_plan_ex(a, None, None) == B.Status.ERR_NULL
+
+
 def test_ex_rejects_bad_options_and_reserved_fields(lib):
     a = B.make_args(FAKE_IN, FAKE_OUT, B.DType.F32, 1, 4, 4, 4, 4)
     assert B.tr_transpose_ex(a, B.make_options(variant=42)) == B.Status.ERR_UNSUPPORTED
