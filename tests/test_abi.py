@@ -271,3 +271,43 @@ def test_bank_probe_argument_errors(lib):
 def test_selftest_argument_errors_on_host(lib):
     assert B.tr_selftest_bounded_wait(0, 0) == B.Status.ERR_BAD_DIM
     assert B.tr_selftest_bounded_wait(1, -5) == B.Status.ERR_BAD_DIM
+
+
+def test_plan_ex_against_the_documented_rules(lib):
+    """Random pointers, shapes and pitches: the planner's aligned sides and
+    AUTO's tile equal a restatement of the header's rules (a side allows
+    16-byte accesses when its base, row pitch and, for batch > 1, plane pitch
+    are multiples of 16 bytes; then the tile follows the table in tr_options)."""
+    import numpy as np
+    rng = np.random.default_rng(7)
+
+    def aligned(base, ld, stride, batch, es):
+        return base % 16 == 0 and (ld * es) % 16 == 0 and (batch == 1 or (stride * es) % 16 == 0)
+
+    def auto_tile(es, in16, out16):
+        v = 16 // es
+        if not in16 and es == 2:
+            return 64, 128, 128
+        if not out16:
+            return 128, 16 * v, 256
+        if not in16:
+            return 16 * v, 128, 256
+        return 16 * v, 16 * v, 256
+
+    for _ in range(3000):
+        dt = B.DType.F32 if rng.random() < 0.5 else B.DType.BF16
+        es = 4 if dt == B.DType.F32 else 2
+        batch = int(rng.choice([1, 1, 2, 5]))
+        rows, cols = int(rng.integers(1, 5000)), int(rng.integers(1, 5000))
+        ld_in, ld_out = cols + int(rng.integers(0, 20)), rows + int(rng.integers(0, 20))
+        si = (rows - 1) * ld_in + cols + int(rng.integers(0, 40))
+        so = (cols - 1) * ld_out + rows + int(rng.integers(0, 40))
+        base_in = FAKE_IN + es * int(rng.integers(0, 8))
+        base_out = FAKE_OUT + es * int(rng.integers(0, 8))
+        st, p = _plan_ex(base_in, base_out, dt, batch, rows, cols, ld_in, ld_out, si, so)
+        assert st == B.Status.OK
+        in16 = aligned(base_in, ld_in, si, batch, es)
+        out16 = aligned(base_out, ld_out, so, batch, es)
+        assert (p.vec_in, p.vec_out) == (in16, out16)
+        assert p.variant == B.Variant.TILE_VEC
+        assert (p.tile_rows, p.tile_cols, p.threads) == auto_tile(es, in16, out16)
