@@ -64,3 +64,44 @@ def first_mismatch(got: np.ndarray, want: np.ndarray) -> str:
     k = bad[0]
     return (f"{bad.size} mismatches, first at flat index {k}: got 0x{int(got[k]):x} "
             f"want 0x{int(want[k]):x}")
+
+
+def oracle_out_banded(x: np.ndarray, out: np.ndarray, batch, rows, cols, ld_in, ld_out, si, so,
+                      threads: int | None = None) -> np.ndarray:
+    """The oracle's transpose of ``x`` into ``out`` (in place), run as one call
+    per batch plane and band of input rows on every host core.  Each call is
+    the oracle's own loop restricted to those rows (input rows r0..r0+n-1 fill
+    output columns r0..r0+n-1 of every output row), so the union of the calls
+    writes exactly what one whole call writes; the loop releases the
+    interpreter lock, so bands run in parallel."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    n = threads or len(os.sched_getaffinity(0))
+    step = max(1, -(-rows // n))
+    jobs = [(b, r0, min(step, rows - r0)) for b in range(batch) for r0 in range(0, rows, step)]
+
+    def one(job):
+        b, r0, nr = job
+        oracle.transpose(x[b * si + r0 * ld_in:], out[b * so + r0:], rows=nr, cols=cols,
+                         ld_in=ld_in, ld_out=ld_out)
+
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        list(pool.map(one, jobs))
+    return out
+
+
+def mismatch_report(got: np.ndarray, want: np.ndarray, chunk: int = 1 << 26) -> str:
+    """Bitwise comparison of two equal-length flat arrays, chunk by chunk (so no
+    full-size temporary is made): "identical" or the count and first mismatch."""
+    assert got.dtype == want.dtype and got.size == want.size
+    count, first = 0, None
+    for s in range(0, got.size, chunk):
+        bad = np.flatnonzero(got[s:s + chunk] != want[s:s + chunk])
+        if bad.size:
+            count += bad.size
+            if first is None:
+                first = s + int(bad[0])
+    if first is None:
+        return "identical"
+    return (f"{count} mismatches, first at flat index {first}: got 0x{int(got[first]):x} "
+            f"want 0x{int(want[first]):x}")

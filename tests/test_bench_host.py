@@ -92,3 +92,48 @@ def test_clock_samples_follow_the_visible_device(monkeypatch):
     assert bench.nvsmi_id(1) == "5"
     monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "")
     assert bench.nvsmi_id(1) == "1"
+
+
+def test_all_core_oracle_baseline_covers_the_plane():
+    """The all-core CPU baseline runs the oracle band by band on several
+    threads; one pass of the bands is the whole transpose."""
+    import numpy as np
+
+    import bench
+    import oracle
+    from shared_memory_tiled_gb300 import workloads as W
+    w = W.WORKLOADS["c1_uniform"]
+    x = W.make_input(w)
+    gbs, secs, desc, threads = bench.time_oracle_all_cores(w, 0.05, x=x, threads=3)
+    assert gbs > 0 and secs >= 0.05 and threads == 3 and "3 bands" in desc
+
+
+def test_config_entry_fields():
+    """A per-configuration entry carries the value, its copy ratio and roofline
+    fraction from the median pass."""
+    import bench
+    from shared_memory_tiled_gb300 import workloads as W
+
+    class Plan:
+        tile_rows, tile_cols, threads, vec_in, vec_out = 64, 64, 256, 1, 1
+
+    class V:
+        name = "TILE_VEC"
+
+    m = bench.Measured()
+    m.w, m.k, m.world = W.WORKLOADS["c2"], 20, 1
+    m.pass_ms = [1.7, 1.6, 1.65, 1.8, 1.62]
+    m.med_ms = 1.65
+    m.ms_step = m.med_ms / m.k
+    m.value = bench.gbps(m.w.algorithmic_bytes * m.k, m.med_ms)
+    m.copy_value = 7000.0
+    m.flush, m.hot_ms = False, None
+    m.planned, m.plan = V(), Plan()
+    m.clocks, m.clock_note = {"sm_mhz": 2070.0}, None
+    e = bench.config_entry(m, 6769.8)
+    assert e["workload"] == "c2" and e["variant"] == "TILE_VEC"
+    assert abs(e["value"] - m.w.algorithmic_bytes * 20 / 1.65e-3 / 1e9) < 0.01
+    assert e["passes_GBps"][0] < e["value"] < e["passes_GBps"][1]
+    assert e["pct_of_copy"] == round(100 * m.value / 7000.0, 2)
+    assert e["roofline_frac"] == round(m.value / 6769.8, 4)
+    assert e["tile"] == "64x64, 256 threads"
