@@ -720,7 +720,7 @@ def run_ours(args):
     tc_ms = statistics.median(gpu.passes(lambda: m.c_out.copy_(m.c_in), args.steps, args.warmup,
                                          args.passes, m.flush))
     torch_copy_gbs = gbps(2 * m.copy_bytes * args.steps * gpu.world, tc_ms)
-    e2e = e2e_measure(gpu, m, max(1, min(args.passes, 3)))
+    e2e = e2e_measure(gpu, m, args.passes)
     head = config_entry(m, peak, inplace)
     kname = {B.Variant.TMA: {1: "k_tma", 3: "k_tma_ldst", 4: "k_tma_ws"}.get(args.schedule, "k_tma_warp"),
              B.Variant.TILE_VEC: "k_tile_vec", B.Variant.TILE_PAD: "k_tile_pad",

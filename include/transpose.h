@@ -295,6 +295,38 @@ tr_status tr_device_status(void);
  * Asynchronous on `stream`. */
 tr_status tr_selftest_bounded_wait(int32_t arrive, int64_t limit_ns, tr_stream_t stream);
 
+/* Record of the bounds checks of a debug build (see tr_debug_bounds). */
+typedef struct tr_bounds_report {
+    int64_t refused;          /* accesses refused since the last read (0 = none)           */
+    uint64_t first_address;   /* device address of one refused access (the first recorded) */
+    int32_t first_bytes;      /* its width in bytes                                        */
+    int32_t first_store;      /* 1 = a store (output side), 0 = a load (input side)        */
+} tr_bounds_report;
+
+/* Debug builds only: the library compiled with TR_DEBUG defined checks every
+ * global load and store of every kernel before making it -- loads against the
+ * input's logical elements (or, for the bf16 loads that realign misaligned
+ * rows on chip, against the input's extent from its first to its last
+ * logical element), stores against the output's logical elements -- and
+ * skips and counts any access that fails ("Shared memory and the bank
+ * conflict", "The barrier": an indexing mistake can leave the result right
+ * most of the time).  Nothing traps.  This call synchronizes the current
+ * device, then fills *report with the accesses refused since the last call
+ * and clears the record.  Returns TR_OK; TR_ERR_UNSUPPORTED (report zeroed)
+ * in a release build, which makes no checks; TR_ERR_NULL for a NULL report;
+ * TR_ERR_CUDA if the device cannot be read. */
+tr_status tr_debug_bounds(tr_bounds_report *report);
+
+/* Debug builds only: tests the guards themselves without touching memory.
+ * One thread asks them about five accesses to a made-up side that it never
+ * dereferences (2 planes of 3 x 5 fp32 elements, row pitch 8, plane pitch
+ * 32, at address `base`): a logical load, a load one column past a row, a
+ * load of the extent's last 16 bytes, a logical 16-byte store and a 16-byte
+ * store that runs two columns past a row.  A following tr_debug_bounds then
+ * reports exactly 2 refusals, the first a 4-byte load at base + 212.
+ * TR_ERR_UNSUPPORTED in a release build; asynchronous on `stream`. */
+tr_status tr_debug_bounds_selftest(uint64_t base, tr_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *tr_status_string(tr_status status);
 

@@ -76,6 +76,11 @@ class Plan(ctypes.Structure):
                 ("vec_out", ctypes.c_int32)]
 
 
+class BoundsReport(ctypes.Structure):
+    _fields_ = [("refused", I64), ("first_address", ctypes.c_uint64),
+                ("first_bytes", ctypes.c_int32), ("first_store", ctypes.c_int32)]
+
+
 class LibraryMissing(RuntimeError):
     pass
 
@@ -104,10 +109,30 @@ SIGNATURES = {
                               ctypes.c_int32, VP], ctypes.c_int),
     "tr_device_status": ([], ctypes.c_int),
     "tr_selftest_bounded_wait": ([ctypes.c_int32, I64, VP], ctypes.c_int),
+    "tr_debug_bounds": ([ctypes.POINTER(BoundsReport)], ctypes.c_int),
+    "tr_debug_bounds_selftest": ([ctypes.c_uint64, VP], ctypes.c_int),
     "tr_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tr_last_error": ([], ctypes.c_char_p),
     "tr_version": ([], ctypes.c_int32),
 }
+
+
+def open_library(path: str):
+    """Open a build of the library at ``path`` (e.g. the bounds-checked one)
+    as its own ctypes handle with every entry point's signature set."""
+    if not os.path.exists(path):
+        raise LibraryMissing(
+            f"libtranspose is not built ({path} missing); run "
+            "`python -m shared_memory_tiled_gb300.build`")
+    try:
+        lib = ctypes.CDLL(path)
+    except OSError as e:  # pragma: no cover - depends on the machine
+        raise LibraryMissing(f"cannot load {path}: {e}") from e
+    for name, (argtypes, restype) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = restype
+    return lib
 
 
 def load(path: str | None = None):
@@ -115,20 +140,7 @@ def load(path: str | None = None):
     global _lib
     with _lock:
         if _lib is None:
-            p = path or LIB_PATH
-            if not os.path.exists(p):
-                raise LibraryMissing(
-                    f"libtranspose is not built ({p} missing); run "
-                    "`python -m shared_memory_tiled_gb300.build`")
-            try:
-                lib = ctypes.CDLL(p)
-            except OSError as e:  # pragma: no cover - depends on the machine
-                raise LibraryMissing(f"cannot load {p}: {e}") from e
-            for name, (argtypes, restype) in SIGNATURES.items():
-                fn = getattr(lib, name)
-                fn.argtypes = argtypes
-                fn.restype = restype
-            _lib = lib
+            _lib = open_library(path or LIB_PATH)
     return _lib
 
 
@@ -205,6 +217,14 @@ def tr_bank_probe(layout, reps, blocks, result_ptr, stream=0) -> int:
 
 def tr_selftest_bounded_wait(arrive, limit_ns, stream=0) -> int:
     return _call("tr_selftest_bounded_wait", arrive, limit_ns, stream)
+
+
+def tr_debug_bounds(report: BoundsReport) -> int:
+    return _call("tr_debug_bounds", ctypes.byref(report) if report is not None else None)
+
+
+def tr_debug_bounds_selftest(base, stream=0) -> int:
+    return _call("tr_debug_bounds_selftest", base, stream)
 
 
 def tr_device_status() -> int:

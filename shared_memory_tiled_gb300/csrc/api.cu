@@ -449,6 +449,40 @@ tr_status tr_device_status(void) {
     return v ? TR_ERR_TIMEOUT : TR_OK;
 }
 
+tr_status tr_debug_bounds(tr_bounds_report *report) {
+    if (!report) return TR_ERR_NULL;
+    *report = tr_bounds_report{};
+    if (!tr::bounds_checked_build()) {
+        tr::set_error("the library was built without bounds checks (TR_DEBUG)", cudaSuccess);
+        return TR_ERR_UNSUPPORTED;
+    }
+    tr::BoundsSummary sum{};
+    const cudaError_t e = tr::read_and_clear_bounds(&sum);
+    if (e != cudaSuccess) {
+        tr::set_error("reading the bounds-check records failed", e);
+        return TR_ERR_CUDA;
+    }
+    report->refused = int64_t(sum.refused);
+    report->first_address = sum.first_addr;
+    report->first_bytes = int32_t(sum.first_bytes);
+    report->first_store = int32_t(sum.first_store);
+    return TR_OK;
+}
+
+tr_status tr_debug_bounds_selftest(uint64_t base, tr_stream_t stream) {
+    if (!tr::bounds_checked_build()) {
+        tr::set_error("the library was built without bounds checks (TR_DEBUG)", cudaSuccess);
+        return TR_ERR_UNSUPPORTED;
+    }
+    const cudaError_t e =
+        tr::launch_bounds_selftest(uintptr_t(base), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tr::set_error("bounds self-test launch failed", e);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
 const char *tr_status_string(tr_status s) {
     switch (s) {
         case TR_OK: return "success";

@@ -15,6 +15,7 @@
 //   3  row pitch 32, but each lane reads along a row: element (c, l) (reference)
 // The tile holds value row*32 + col at every logical position, so the folded
 // result of each thread is known in closed form.
+#include "bounds.cuh"
 #include "tr_internal.h"
 
 namespace tr {
@@ -42,10 +43,15 @@ __global__ void __launch_bounds__(256) k_bank_probe(int reps, uint32_t *result) 
         const uint32_t v = LAYOUT == 3 ? tile[c * 32 + lane] : tile[probe_word<LAYOUT>(lane, c)];
         acc = ((acc << 1) | (acc >> 31)) ^ v;  // rotate-and-fold: no two reads cancel
     }
-    result[size_t(blockIdx.x) * blockDim.x + threadIdx.x] = acc;
+    uint32_t *slot = result + size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    TR_SIDE(out_side, result, 1, 1, int64_t(gridDim.x) * blockDim.x, int64_t(gridDim.x) * blockDim.x, 0, 4);
+    if (TR_STORE_OK(out_side, slot, 4)) *slot = acc;
 }
 
 }  // namespace
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_bank_probe)
 
 cudaError_t launch_bank_probe(int layout, int reps, int blocks, uint32_t *result,
                               cudaStream_t stream) {

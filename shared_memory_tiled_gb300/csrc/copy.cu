@@ -3,6 +3,7 @@
 // section "What to record": the transpose sits next to a copy of the same
 // bytes).  Moving N bytes costs N bytes read plus N bytes written, exactly the
 // algorithmic traffic of a transpose of N bytes.
+#include "bounds.cuh"
 #include "launch.cuh"
 #include "tr_internal.h"
 
@@ -20,10 +21,24 @@ __global__ void __launch_bounds__(kThreads)
 k_copy_aligned(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int head,
                int64_t n16, int tail) {
     pdl_prologue();
+    // Debug builds: both ranges as one row of head + 16*n16 + tail bytes.
+    TR_SIDE(in_side, in, 1, 1, head + n16 * 16 + tail, head + n16 * 16 + tail, 0, 1);
+    TR_SIDE(out_side, out, 1, 1, head + n16 * 16 + tail, head + n16 * 16 + tail, 0, 1);
+    auto ld = [&](const uint4 *p) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (TR_LOAD_OK(in_side, p, 16)) v = __ldcs(p);
+        return v;
+    };
+    auto st = [&](uint4 *p, uint4 v) {
+        if (TR_STORE_OK(out_side, p, 16)) __stcs(p, v);
+    };
+    auto move1 = [&](int64_t i) {
+        if (TR_LOAD_OK(in_side, in + i, 1) && TR_STORE_OK(out_side, out + i, 1)) out[i] = in[i];
+    };
     if (blockIdx.x == 0) {
-        if (threadIdx.x < head) out[threadIdx.x] = in[threadIdx.x];
+        if (threadIdx.x < head) move1(threadIdx.x);
         const int64_t t0 = head + n16 * 16;
-        if (threadIdx.x < tail) out[t0 + threadIdx.x] = in[t0 + threadIdx.x];
+        if (threadIdx.x < tail) move1(t0 + threadIdx.x);
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(in + head);
     uint4 *dst = reinterpret_cast<uint4 *>(out + head);
@@ -33,19 +48,19 @@ k_copy_aligned(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int he
         uint4 v[kUnroll];
         if (base + per_turn <= n16) {
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) v[k] = __ldcs(src + base + k * kThreads + threadIdx.x);
+            for (int k = 0; k < kUnroll; ++k) v[k] = ld(src + base + k * kThreads + threadIdx.x);
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) __stcs(dst + base + k * kThreads + threadIdx.x, v[k]);
+            for (int k = 0; k < kUnroll; ++k) st(dst + base + k * kThreads + threadIdx.x, v[k]);
         } else {
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
                 const int64_t idx = base + k * kThreads + threadIdx.x;
-                if (idx < n16) v[k] = __ldcs(src + idx);
+                if (idx < n16) v[k] = ld(src + idx);
             }
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
                 const int64_t idx = base + k * kThreads + threadIdx.x;
-                if (idx < n16) __stcs(dst + idx, v[k]);
+                if (idx < n16) st(dst + idx, v[k]);
             }
         }
     }
@@ -58,16 +73,24 @@ __global__ void __launch_bounds__(kThreads)
 k_copy_narrow(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int head, int64_t nw,
               int tail) {
     pdl_prologue();
+    const int64_t n = head + nw * int64_t(sizeof(W)) + tail;
+    TR_SIDE(in_side, in, 1, 1, n, n, 0, 1);
+    TR_SIDE(out_side, out, 1, 1, n, n, 0, 1);
+    auto move1 = [&](int64_t i) {
+        if (TR_LOAD_OK(in_side, in + i, 1) && TR_STORE_OK(out_side, out + i, 1)) out[i] = in[i];
+    };
     if (blockIdx.x == 0) {
-        if (threadIdx.x < head) out[threadIdx.x] = in[threadIdx.x];
+        if (threadIdx.x < head) move1(threadIdx.x);
         const int64_t t0 = head + nw * int64_t(sizeof(W));
-        if (threadIdx.x < tail) out[t0 + threadIdx.x] = in[t0 + threadIdx.x];
+        if (threadIdx.x < tail) move1(t0 + threadIdx.x);
     }
     const W *src = reinterpret_cast<const W *>(in + head);
     W *dst = reinterpret_cast<W *>(out + head);
     for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < nw;
          idx += int64_t(gridDim.x) * kThreads)
-        dst[idx] = src[idx];
+        if (TR_LOAD_OK(in_side, src + idx, int(sizeof(W))) &&
+            TR_STORE_OK(out_side, dst + idx, int(sizeof(W))))
+            dst[idx] = src[idx];
 }
 
 int64_t grid_for(int64_t units, int64_t per_block) {
@@ -78,6 +101,9 @@ int64_t grid_for(int64_t units, int64_t per_block) {
 }
 
 }  // namespace
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_copy)
 
 cudaError_t launch_copy(const void *in_, void *out_, size_t bytes, cudaStream_t stream) {
     const uint8_t *in = static_cast<const uint8_t *>(in_);

@@ -16,6 +16,7 @@
 //
 // Blocks walk a batch * T * T grid of tile coordinates (T tiles per side) and
 // skip the lower triangle, so each pair is taken exactly once.
+#include "bounds.cuh"
 #include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
     const int t = threadIdx.x;
     const int lcc = t & 15, lr = t >> 4;  // phase 1: chunk and first row
     const int A = t & 15, C = t >> 4;     // phase 2: micro-block
+    // Debug builds: every load and store must touch logical elements only.
+    TR_SIDE(side, data, g.batch, g.n, g.n, g.ld, g.stride, int(sizeof(T)));
 
     bool first = true;
     for (int64_t w = blockIdx.x; w < g.total; w += gridDim.x) {
@@ -81,12 +84,17 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
             for (int k = 0; k < LOADS; ++k) {
                 const int64_t gr = rr0 + lr + 16 * k;
                 if (VEC && (full || (gr < g.n && gc + V <= g.n))) {
-                    ld[k].v = *reinterpret_cast<const uint4 *>(plane + gr * g.ld + gc);
+                    const T *p = plane + gr * g.ld + gc;
+                    ld[k].v = TR_LOAD_OK(side, p, 16) ? *reinterpret_cast<const uint4 *>(p)
+                                                      : make_uint4(0u, 0u, 0u, 0u);
                 } else {
                     T e[V];
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        e[q] = (gr < g.n && gc + q < g.n) ? plane[gr * g.ld + gc + q] : T(0);
+                        e[q] = (gr < g.n && gc + q < g.n &&
+                                TR_LOAD_OK(side, plane + gr * g.ld + gc + q, int(sizeof(T))))
+                                   ? plane[gr * g.ld + gc + q]
+                                   : T(0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if constexpr (sizeof(T) == 4)
@@ -142,11 +150,13 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
                 if (!full && orow >= g.n) break;
                 T *row = plane + orow * g.ld;
                 if (VEC && (full || oc + V <= g.n)) {
-                    __stcs(reinterpret_cast<uint4 *>(row + oc), yv[m].v);  // streaming store
+                    if (TR_STORE_OK(side, row + oc, 16))
+                        __stcs(reinterpret_cast<uint4 *>(row + oc), yv[m].v);  // streaming store
                 } else {
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        if (oc + q < g.n) row[oc + q] = elem<T>(yv[m], q);
+                        if (oc + q < g.n && TR_STORE_OK(side, row + oc + q, int(sizeof(T))))
+                            row[oc + q] = elem<T>(yv[m], q);
                 }
             }
         };
@@ -180,6 +190,9 @@ cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
 }
 
 }  // namespace
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_inplace)
 
 cudaError_t launch_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
                            int64_t stride, cudaStream_t stream) {

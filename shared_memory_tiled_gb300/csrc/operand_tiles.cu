@@ -18,6 +18,7 @@
 //
 // The output exists so the stage has a checkable result and so its shared
 // stores can be measured (bank-conflict counters) apart from any arithmetic.
+#include "bounds.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
 
@@ -37,13 +38,18 @@ k_operand_tiles(const uint32_t *__restrict__ a, uint32_t *__restrict__ out, int6
     const int t = threadIdx.x;
     const int inner_row = t / COLS4, inner_col = t % COLS4;
     const int64_t total = m_tiles * k_tiles;
+    // Debug builds: A is M x K at pitch lda; the output holds M*K words.
+    TR_SIDE(in_side, a, 1, m_tiles * BM, k_tiles * BK, lda, 0, 4);
+    TR_SIDE(out_side, out, 1, 1, total * BM * BK, total * BM * BK, 0, 4);
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
         const int64_t mt = tile / k_tiles, kt = tile - mt * k_tiles;
         const uint32_t *src = a + (mt * BM) * lda + kt * BK + inner_col * 4;
         if (tile != blockIdx.x) __syncthreads();  // previous tile written out
 #pragma unroll
         for (int off = 0; off < BM; off += ROW_STRIDE) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + (inner_row + off) * lda);
+            const uint32_t *p = src + (inner_row + off) * lda;
+            const uint4 v = TR_LOAD_OK(in_side, p, 16) ? *reinterpret_cast<const uint4 *>(p)
+                                                       : make_uint4(0u, 0u, 0u, 0u);
             uint32_t *col = as + (inner_col * 4) * a_stride + inner_row + off;
             col[0] = v.x;
             col[a_stride] = v.y;
@@ -53,7 +59,8 @@ k_operand_tiles(const uint32_t *__restrict__ a, uint32_t *__restrict__ out, int6
         __syncthreads();
         uint32_t *dst = out + tile * (BM * BK);
 #pragma unroll 4
-        for (int w = t; w < BM * BK; w += kThreads) dst[w] = as[(w / BM) * a_stride + (w % BM)];
+        for (int w = t; w < BM * BK; w += kThreads)
+            if (TR_STORE_OK(out_side, dst + w, 4)) dst[w] = as[(w / BM) * a_stride + (w % BM)];
     }
 }
 
@@ -69,6 +76,9 @@ cudaError_t launch_shape(const uint32_t *a, uint32_t *out, int64_t m, int64_t k,
 }
 
 }  // namespace
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_operand_tiles)
 
 cudaError_t launch_operand_tiles(const uint32_t *a, uint32_t *out, int64_t m, int64_t k,
                                  int64_t lda, int bm, int bk, int pad, cudaStream_t stream) {

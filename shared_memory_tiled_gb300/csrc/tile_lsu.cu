@@ -6,6 +6,7 @@
 // All index arithmetic is 64-bit; tiles are walked through a 1-D grid whose
 // block index is split into (plane, tile row, tile column), tile column
 // fastest, with a grid-stride loop for problems beyond the grid limit.
+#include "bounds.cuh"
 #include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
@@ -24,6 +25,11 @@ template <typename T, bool READ_ROWS>
 __global__ void __launch_bounds__(256) k_naive(const T *__restrict__ in, T *__restrict__ out,
                                                Geometry g) {
     pdl_prologue();
+    TR_SIDE(in_side, in, g.batch, g.rows, g.cols, g.ld_in, g.stride_in, int(sizeof(T)));
+    TR_SIDE(out_side, out, g.batch, g.cols, g.rows, g.ld_out, g.stride_out, int(sizeof(T)));
+    auto move = [&](T *d, const T *s) {
+        if (TR_LOAD_OK(in_side, s, int(sizeof(T))) && TR_STORE_OK(out_side, d, int(sizeof(T)))) *d = *s;
+    };
     for (int64_t t = blockIdx.x; t < g.total; t += gridDim.x) {
         int64_t b, tr, tc;
         split_tile(g, t, false, b, tr, tc);
@@ -34,14 +40,14 @@ __global__ void __launch_bounds__(256) k_naive(const T *__restrict__ in, T *__re
 #pragma unroll
             for (int k = 0; k < 32; k += 8) {
                 const int64_t i = tr * 32 + threadIdx.y + k;  // input row
-                if (i < g.rows && j < g.cols) dst[j * g.ld_out + i] = src[i * g.ld_in + j];
+                if (i < g.rows && j < g.cols) move(dst + j * g.ld_out + i, src + i * g.ld_in + j);
             }
         } else {
             const int64_t i = tr * 32 + threadIdx.x;          // output column
 #pragma unroll
             for (int k = 0; k < 32; k += 8) {
                 const int64_t j = tc * 32 + threadIdx.y + k;  // output row
-                if (i < g.rows && j < g.cols) dst[j * g.ld_out + i] = src[i * g.ld_in + j];
+                if (i < g.rows && j < g.cols) move(dst + j * g.ld_out + i, src + i * g.ld_in + j);
             }
         }
     }
@@ -65,6 +71,8 @@ __global__ void __launch_bounds__(256) k_tile_pad(const T *__restrict__ in, T *_
     __shared__ T tile[32][32 + PAD];
     pdl_prologue();
     const int tx = threadIdx.x, ty = threadIdx.y;
+    TR_SIDE(in_side, in, g.batch, g.rows, g.cols, g.ld_in, g.stride_in, int(sizeof(T)));
+    TR_SIDE(out_side, out, g.batch, g.cols, g.rows, g.ld_out, g.stride_out, int(sizeof(T)));
     for (int64_t t = blockIdx.x; t < g.total; t += gridDim.x) {
         int64_t b, tr, tc;
         split_tile(g, t, false, b, tr, tc);
@@ -75,13 +83,15 @@ __global__ void __launch_bounds__(256) k_tile_pad(const T *__restrict__ in, T *_
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
             const int64_t i = r0 + ty + k, j = c0 + tx;
-            if (i < g.rows && j < g.cols) tile[ty + k][tx] = src[i * g.ld_in + j];
+            if (i < g.rows && j < g.cols && TR_LOAD_OK(in_side, src + i * g.ld_in + j, int(sizeof(T))))
+                tile[ty + k][tx] = src[i * g.ld_in + j];
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
             const int64_t j = c0 + ty + k, i = r0 + tx;   // output row j, column i
-            if (i < g.rows && j < g.cols) dst[j * g.ld_out + i] = tile[tx][ty + k];
+            if (i < g.rows && j < g.cols && TR_STORE_OK(out_side, dst + j * g.ld_out + i, int(sizeof(T))))
+                dst[j * g.ld_out + i] = tile[tx][ty + k];
         }
     }
 }
@@ -119,6 +129,9 @@ cudaError_t launch_naive_typed(const Problem &p, bool read_rows) {
 }
 
 }  // namespace
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_lsu)
 
 cudaError_t launch_naive(const Problem &p, bool read_coalesced) {
     return p.esize == 4 ? launch_naive_typed<uint32_t>(p, read_coalesced)

@@ -42,6 +42,7 @@
 // micro-block with bounds-checked element stores.  Input rows need no such
 // care: extra elements a load brings in land in output rows past `cols`, which
 // the store clips (whole lines).
+#include "bounds.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
 #include "tr_internal.h"
@@ -75,6 +76,20 @@ struct TmaGeom {
     void *out;            // output base, for those element stores
     int64_t ld_out, stride_out;
 };
+
+// Global stores made with the LSU (the TMA boxes themselves are clipped to the
+// tensor maps by the hardware).  Debug builds check each against the logical
+// output elements first.
+template <typename T>
+__device__ __forceinline__ dbg::Side out_side(const TmaGeom &g) {
+    return dbg::side(g.out, g.total / (int64_t(g.tiles_r) * g.tiles_c), g.cols, g.rows, g.ld_out,
+                     g.stride_out, int(sizeof(T)));
+}
+
+template <typename T>
+__device__ __forceinline__ void store_chunk(const TmaGeom &g, T *p, uint4 v) {
+    if (TR_STORE_OK(out_side<T>(g), p, 16)) __stcs(reinterpret_cast<uint4 *>(p), v);
+}
 
 template <typename T>
 struct TmaTile {
@@ -184,7 +199,9 @@ k_tma(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtenso
                 if (orow < g.cols) {
 #pragma unroll
                     for (int e = 0; e < V; ++e)
-                        if (oc + e < g.rows) dst[orow * g.ld_out + oc + e] = elem<T>(y[m], e);
+                        if (oc + e < g.rows &&
+                            TR_STORE_OK(out_side<T>(g), dst + orow * g.ld_out + oc + e, int(sizeof(T))))
+                            dst[orow * g.ld_out + oc + e] = elem<T>(y[m], e);
                 }
             }
         }
@@ -331,7 +348,9 @@ k_tma_warp(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CU
                     if (orow < g.cols) {
 #pragma unroll
                         for (int e = 0; e < V; ++e)
-                            if (oc + e < g.rows) dst[orow * g.ld_out + oc + e] = elem<T>(yv[m], e);
+                            if (oc + e < g.rows &&
+                                TR_STORE_OK(out_side<T>(g), dst + orow * g.ld_out + oc + e, int(sizeof(T))))
+                                dst[orow * g.ld_out + oc + e] = elem<T>(yv[m], e);
                     }
                 }
             }
@@ -473,14 +492,15 @@ k_tma_ldst(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
                 const int64_t orow = c0 + V * C + m;
                 T *row = dst + orow * g.ld_out;
                 if (full_tile) {
-                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                    store_chunk<T>(g, row + oc, y[m].v);
                 } else if (orow < g.cols) {
                     if (oc + V <= g.rows) {
-                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                        store_chunk<T>(g, row + oc, y[m].v);
                     } else {
 #pragma unroll
                         for (int e = 0; e < V; ++e)
-                            if (oc + e < g.rows) row[oc + e] = elem<T>(y[m], e);
+                            if (oc + e < g.rows && TR_STORE_OK(out_side<T>(g), row + oc + e, int(sizeof(T))))
+                            row[oc + e] = elem<T>(y[m], e);
                     }
                 }
             }
@@ -617,14 +637,15 @@ k_tma_ws(const __grid_constant__ CUtensorMap tm_in, TmaGeom g) {
             const int64_t orow = c0 + V * C + m;
             T *row = dst + orow * g.ld_out;
             if (full_tile) {
-                __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                store_chunk<T>(g, row + oc, y[m].v);
             } else if (orow < g.cols) {
                 if (oc + V <= g.rows) {
-                    __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                    store_chunk<T>(g, row + oc, y[m].v);
                 } else {
 #pragma unroll
                     for (int e = 0; e < V; ++e)
-                        if (oc + e < g.rows) row[oc + e] = elem<T>(y[m], e);
+                        if (oc + e < g.rows && TR_STORE_OK(out_side<T>(g), row + oc + e, int(sizeof(T))))
+                            row[oc + e] = elem<T>(y[m], e);
                 }
             }
         }
@@ -895,6 +916,9 @@ cudaError_t launch_wait_selftest(bool arrive, int64_t limit_ns, cudaStream_t str
     k_wait_selftest<<<1, 32, 0, stream>>>(arrive ? 1 : 0, uint64_t(limit_ns));
     return cudaGetLastError();
 }
+
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_tma)
 
 cudaError_t read_and_clear_fault(unsigned *value) {
     cudaError_t e = cudaDeviceSynchronize();

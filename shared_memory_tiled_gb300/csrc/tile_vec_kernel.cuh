@@ -55,6 +55,7 @@
 // missing.
 #pragma once
 
+#include "bounds.cuh"
 #include "launch.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
@@ -130,6 +131,18 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
     pdl_prologue();
     const int t = threadIdx.x;
     const int lcc = t % MC, lr = t / MC;
+    // Debug builds: the two sides every global access is checked against.
+    TR_SIDE(in_side, in, g.batch, g.rows, g.cols, g.ld_in, g.stride_in, int(sizeof(T)));
+    TR_SIDE(out_side, out, g.batch, g.cols, g.rows, g.ld_out, g.stride_out, int(sizeof(T)));
+    // 16-byte global accesses (streaming loads and stores).
+    auto ld16 = [&](const void *p) {
+        return TR_LOAD_OK(in_side, p, 16) ? __ldcs(reinterpret_cast<const uint4 *>(p))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto st16 = [&](T *p, uint4 v) {
+        if (TR_STORE_OK(out_side, p, 16)) __stcs(reinterpret_cast<uint4 *>(p), v);
+    };
+
     // Whether tile (b, tr, tc) takes the aligned-chunk path.
     auto raw_tile = [&](bool full, int64_t b, int64_t tr, int64_t tc) {
         const int64_t end = (tr + 1) * TR + HALO;  // one past the last row read
@@ -137,8 +150,9 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
         const bool last = b == g.batch - 1 && end >= g.rows && (tc + 1) * TC + V > g.cols;
         return RAW && full && end <= g.rows && !first && !last;
     };
-    auto aligned_chunk = [](const T *p) {
-        return __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15)));
+    auto aligned_chunk = [&](const T *p) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15));
+        return TR_LOAD_IN_EXTENT(in_side, q, 16) ? __ldcs(q) : make_uint4(0u, 0u, 0u, 0u);
     };
 
     // Phase 1a: this thread's chunks of tile `tile`, global -> registers, all
@@ -176,20 +190,22 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
         if (full && VEC_IN) {
 #pragma unroll
             for (int k = 0; k < LOADS; ++k)
-                ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + (r0 + lr + RPP * k) * g.ld_in + gc));
+                ld[k].v = ld16(src + (r0 + lr + RPP * k) * g.ld_in + gc);
         } else if (!raw) {
 #pragma unroll
             for (int k = 0; k < LOADS; ++k) {
                 const int64_t gr = r0 + lr + RPP * k;
                 if (VEC_IN && gr < g.rows && gc + V <= g.cols) {
-                    ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + gc));
+                    ld[k].v = ld16(src + gr * g.ld_in + gc);
                 } else if (!VEC_IN && gr < g.rows && gc + V <= g.cols) {
                     // A whole chunk in range on a misaligned side (row starts
                     // differ from row to row): the widest loads this chunk's
                     // own address allows, touching only its own elements.
                     const T *p = src + gr * g.ld_in + gc;
                     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-                    if ((a & 15u) == 0) {
+                    if (!TR_LOAD_OK(in_side, p, 16)) {
+                        ld[k].v = make_uint4(0u, 0u, 0u, 0u);
+                    } else if ((a & 15u) == 0) {
                         ld[k].v = __ldcs(reinterpret_cast<const uint4 *>(p));
                     } else if ((a & 7u) == 0) {
                         const uint2 lo = __ldcs(reinterpret_cast<const uint2 *>(p));
@@ -208,7 +224,10 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     T e[V];
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        e[q] = (gr < g.rows && gc + q < g.cols) ? src[gr * g.ld_in + gc + q] : T(0);
+                        e[q] = (gr < g.rows && gc + q < g.cols &&
+                                TR_LOAD_OK(in_side, src + gr * g.ld_in + gc + q, int(sizeof(T))))
+                                   ? src[gr * g.ld_in + gc + q]
+                                   : T(0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if constexpr (sizeof(T) == 4)
@@ -231,12 +250,15 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                 if (raw) {
                     hl[k].v = aligned_chunk(src + gr * g.ld_in + hc);
                 } else if (VEC_IN && gr < g.rows && hc + V <= g.cols) {
-                    hl[k].v = __ldcs(reinterpret_cast<const uint4 *>(src + gr * g.ld_in + hc));
+                    hl[k].v = ld16(src + gr * g.ld_in + hc);
                 } else {
                     T e[V];
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        e[q] = (gr < g.rows && hc + q < g.cols) ? src[gr * g.ld_in + hc + q] : T(0);
+                        e[q] = (gr < g.rows && hc + q < g.cols &&
+                                TR_LOAD_OK(in_side, src + gr * g.ld_in + hc + q, int(sizeof(T))))
+                                   ? src[gr * g.ld_in + hc + q]
+                                   : T(0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if constexpr (sizeof(T) == 4)
@@ -349,8 +371,7 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
             const int64_t oc = r0 + V * A;  // first output column of this lane's chunk
             if (full && !SHIFT_OUT) {
 #pragma unroll
-                for (int m = 0; m < V; ++m)
-                    __stcs(reinterpret_cast<uint4 *>(dst + (c0 + V * C + m) * g.ld_out + oc), y[m].v);
+                for (int m = 0; m < V; ++m) st16(dst + (c0 + V * C + m) * g.ld_out + oc, y[m].v);
             } else if (SHIFT_OUT && r0 + TR <= g.rows) {
                 // Every output row segment of the tile is complete (the tile may
                 // still stop short of the last output rows).  For an output row
@@ -387,24 +408,26 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
                     const int d = (V - s) % V;  // elements before the first 16-byte boundary
                     if (d == 0) {
-                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                        st16(row + oc, y[m].v);
                         continue;
                     }
                     const int64_t wc = oc + d;  // first column of the aligned chunk
                     Chunk wv;
                     wv.v = window<T>(y[m], nb, d);
                     if (wc + V <= g.rows) {
-                        __stcs(reinterpret_cast<uint4 *>(row + wc), wv.v);
+                        st16(row + wc, wv.v);
                     } else {
                         // the halo ran past the last input row
 #pragma unroll
                         for (int q = 0; q < V; ++q)
-                            if (wc + q < g.rows) row[wc + q] = elem<T>(wv, q);
+                            if (wc + q < g.rows && TR_STORE_OK(out_side, row + wc + q, int(sizeof(T))))
+                                row[wc + q] = elem<T>(wv, q);
                     }
                     if (tr == 0 && A == 0) {
 #pragma unroll
                         for (int q = 0; q < V; ++q)
-                            if (q < d) row[q] = elem<T>(y[m], q);
+                            if (q < d && TR_STORE_OK(out_side, row + q, int(sizeof(T))))
+                                row[q] = elem<T>(y[m], q);
                     }
                 }
             } else {
@@ -414,7 +437,7 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                     if (orow >= g.cols) break;
                     T *row = dst + orow * g.ld_out;
                     if (!SHIFT_OUT && oc + V <= g.rows) {
-                        __stcs(reinterpret_cast<uint4 *>(row + oc), y[m].v);
+                        st16(row + oc, y[m].v);
                     } else {
                         // With shifted stores the first d columns of the segment
                         // belong to the tile above (it wrote them from its halo).
@@ -427,7 +450,9 @@ __global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__
                         }
 #pragma unroll
                         for (int q = 0; q < V; ++q)
-                            if (oc + q < g.rows && oc + q >= lo) row[oc + q] = elem<T>(y[m], q);
+                            if (oc + q < g.rows && oc + q >= lo &&
+                                TR_STORE_OK(out_side, row + oc + q, int(sizeof(T))))
+                                row[oc + q] = elem<T>(y[m], q);
                     }
                 }
             }

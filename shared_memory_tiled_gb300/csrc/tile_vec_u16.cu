@@ -8,4 +8,7 @@ cudaError_t launch_vec_u16(const Problem &p, bool vec_in, bool vec_out, const Ve
     return vec::launch_typed<uint16_t, false>(p, vec_in, vec_out, cfg, why);
 }
 
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_vec_u16)
+
 }  // namespace tr

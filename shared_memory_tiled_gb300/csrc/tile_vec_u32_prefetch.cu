@@ -8,4 +8,7 @@ cudaError_t launch_vec_u32_prefetch(const Problem &p, bool vec_in, bool vec_out,
     return vec::launch_typed<uint32_t, true>(p, vec_in, vec_out, cfg, why);
 }
 
+// Debug builds: this unit's record of refused accesses.
+TR_BOUNDS_READER(read_bounds_vec_u32_prefetch)
+
 }  // namespace tr

@@ -74,4 +74,19 @@ cudaError_t read_and_clear_fault(unsigned *value);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Debug-build bounds checks (bounds.cuh): the merged record of every unit.
+struct BoundsSummary {
+    unsigned long long refused;     // accesses refused since the last read
+    unsigned long long first_addr;  // one refused access (the first a unit recorded)
+    unsigned first_bytes;
+    unsigned first_store;
+};
+// Whether the library was compiled with the checks (TR_DEBUG).
+bool bounds_checked_build();
+// Synchronizes the current device, then reads and clears every unit's record.
+cudaError_t read_and_clear_bounds(BoundsSummary *sum);
+// The guards' self-test (debug builds; cudaErrorNotSupported otherwise):
+// `base` is a made-up address the kernel never dereferences.
+cudaError_t launch_bounds_selftest(uintptr_t base, cudaStream_t stream);
+
 }  // namespace tr

@@ -33,8 +33,13 @@ def oracle_out(x: np.ndarray, prefill: np.ndarray, batch, rows, cols, ld_in, ld_
 
 
 def gpu_out(x: np.ndarray, prefill: np.ndarray, batch, rows, cols, ld_in, ld_out, si, so,
-            variant=B.Variant.AUTO, in_off=0, out_off=0, entry="ex", stream=0, **opt):
-    """Transpose on the GPU through the C ABI; returns the whole output buffer."""
+            variant=B.Variant.AUTO, in_off=0, out_off=0, entry="ex", stream=0, lib=None, **opt):
+    """Transpose on the GPU through the C ABI; returns the whole output buffer.
+    ``lib`` is a library handle from ``binding.open_library`` (another build of
+    the library, e.g. the bounds-checked one), used with entry="ex"; default:
+    the binding's own library."""
+    import ctypes
+
     import torch
     dt = B.DType.F32 if x.dtype == np.uint32 else B.DType.BF16
     dev_in, p_in = to_device(x, in_off)
@@ -42,7 +47,9 @@ def gpu_out(x: np.ndarray, prefill: np.ndarray, batch, rows, cols, ld_in, ld_out
     torch.cuda.synchronize()
     if entry == "ex":
         args = B.make_args(p_in, p_out, dt, batch, rows, cols, ld_in, ld_out, si, so, stream)
-        st = B.tr_transpose_ex(args, B.make_options(variant, **opt))
+        opts = B.make_options(variant, **opt)
+        st = (lib.tr_transpose_ex(ctypes.byref(args), ctypes.byref(opts)) if lib is not None
+              else B.tr_transpose_ex(args, opts))
     elif entry == "plain":
         assert batch == 1
         f = B.tr_transpose_f32 if dt == B.DType.F32 else B.tr_transpose_bf16
@@ -52,6 +59,8 @@ def gpu_out(x: np.ndarray, prefill: np.ndarray, batch, rows, cols, ld_in, ld_out
         st = f(p_in, p_out, batch, rows, cols, ld_in, ld_out, si, so, stream)
     else:
         raise ValueError(entry)
+    if st != B.Status.OK and lib is not None:
+        raise B.TransposeError(st, lib.tr_last_error().decode())
     B.check(st)
     torch.cuda.synchronize()
     return from_device(dev_out, prefill.size, out_off, x.dtype.type)

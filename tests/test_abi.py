@@ -311,3 +311,14 @@ def test_plan_ex_against_the_documented_rules(lib):
         assert (p.vec_in, p.vec_out) == (in16, out16)
         assert p.variant == B.Variant.TILE_VEC
         assert (p.tile_rows, p.tile_cols, p.threads) == auto_tile(es, in16, out16)
+
+
+def test_release_build_makes_no_bounds_checks(lib):
+    """The release library has no bounds checks: both debug entry points say so
+    on the host, without a CUDA call, and a NULL report is an argument error."""
+    rep = B.BoundsReport(refused=5)
+    assert B.tr_debug_bounds(rep) == B.Status.ERR_UNSUPPORTED
+    assert rep.refused == 0
+    assert "TR_DEBUG" in B.tr_last_error()
+    assert B.tr_debug_bounds(None) == B.Status.ERR_NULL
+    assert B.tr_debug_bounds_selftest(0x10000) == B.Status.ERR_UNSUPPORTED
