@@ -71,15 +71,17 @@ def read_peaks():
 # Source files each kernel is built from (the hash of these decides whether a
 # recorded ncu traffic figure still describes the kernel that runs).
 KERNEL_SOURCES = {
-    "k_tile_vec": ["tile_vec_kernel.cuh", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h"],
-    "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
-    "k_tma_warp": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
-    "k_tma_ldst": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
-    "k_tma_ws": ["tile_tma.cu", "ptx.cuh", "tr_internal.h"],
-    "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
-    "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h"],
-    "k_copy_aligned": ["copy.cu", "tr_internal.h"],
-    "k_inplace": ["inplace.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h"],
+    "k_tile_vec": ["tile_vec_kernel.cuh", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h",
+                   "bounds.cuh"],
+    "k_tma": ["tile_tma.cu", "ptx.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_tma_warp": ["tile_tma.cu", "ptx.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_tma_ldst": ["tile_tma.cu", "ptx.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_tma_ws": ["tile_tma.cu", "ptx.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_tile_pad": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h", "bounds.cuh"],
+    "k_copy_aligned": ["copy.cu", "tr_internal.h", "bounds.cuh"],
+    "k_inplace": ["inplace.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h",
+                  "bounds.cuh"],
 }
 
 
