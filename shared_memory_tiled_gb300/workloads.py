@@ -27,6 +27,8 @@ The workloads follow the five configurations the library is measured on:
   start at every 4-byte offset from a 16-byte boundary) and output pitch 7936.
 * ``c5_oddin``   c5 with input pitch 16385 (bf16 rows start at every 2-byte
   offset from a 16-byte boundary), output dense.
+* ``c5_oddout``  c5 with output pitch 16385; ``c5_oddboth`` with both pitches
+  16385; ``c2_oddout`` c2 with output pitch 8193.
 """
 from __future__ import annotations
 
@@ -110,6 +112,11 @@ WORKLOADS = {
     "c3_back": Workload("c3_back", "f32", 7919, 12289, 12289, 7936, dist="normal", seed=2),
     # c5 with the odd pitch on the input side
     "c5_oddin": Workload("c5_oddin", "bf16", 16384, 16384, 16385, 16384, dist="bits", seed=4),
+    # c5 with an odd output pitch (shifted stores), and with both pitches odd
+    "c5_oddout": Workload("c5_oddout", "bf16", 16384, 16384, 16384, 16385, dist="bits", seed=4),
+    "c5_oddboth": Workload("c5_oddboth", "bf16", 16384, 16384, 16385, 16385, dist="bits", seed=4),
+    # c2 with an odd output pitch
+    "c2_oddout": Workload("c2_oddout", "f32", 8192, 8192, 8192, 8193, dist="uniform", seed=1),
 }
 
 DESCRIPTION = {
@@ -121,6 +128,9 @@ DESCRIPTION = {
     "c5": "bf16 16384x16384 (512 MiB) square, uniform random u16 bits seed 4",
     "c3_back": "fp32 7919x12289 (c3's output shape), input pitch 12289, output pitch 7936, N(0,1) seed 2",
     "c5_oddin": "bf16 16384x16384, input pitch 16385, output dense, uniform random u16 bits seed 4",
+    "c5_oddout": "bf16 16384x16384, input dense, output pitch 16385, uniform random u16 bits seed 4",
+    "c5_oddboth": "bf16 16384x16384, input and output pitch 16385, uniform random u16 bits seed 4",
+    "c2_oddout": "fp32 8192x8192, input dense, output pitch 8193, uniform[-1,1) seed 1",
 }
 
 
