@@ -81,7 +81,7 @@ KERNEL_SOURCES = {
     "k_naive": ["tile_lsu.cu", "tile_geom.cuh", "tr_internal.h", "bounds.cuh"],
     "k_copy_aligned": ["copy.cu", "tr_internal.h", "bounds.cuh"],
     "k_inplace": ["inplace.cu", "vec_common.cuh", "tile_geom.cuh", "tr_internal.h",
-                  "bounds.cuh"],
+                  "bounds.cuh", "ptx.cuh"],
 }
 
 

@@ -2,11 +2,13 @@
 //
 // The out-of-place kernels read one tile and write its transpose elsewhere.
 // In place, the transpose of tile (ti, tj) lands where tile (tj, ti) lives, so
-// one block owns each unordered pair of tiles: it reads BOTH tiles (through
-// registers) into two swizzled shared tiles, and only after the barrier writes
-// each one's transpose over the other ("Shared memory and the bank conflict",
-// "The barrier": nothing may be written before every thread's reads are in).  A diagonal tile is its own partner.  No other block reads or
-// writes either tile, so blocks never race.
+// one block owns each unordered pair of tiles: it reads BOTH tiles into two
+// swizzled shared tiles (whole tiles by asynchronous 16-byte copies, edge
+// tiles through registers), and only after the barrier writes each one's
+// transpose over the other ("Shared memory and the bank conflict", "The
+// barrier": nothing may be written before every thread's reads are in).  A
+// diagonal tile is its own partner.  No other block reads or writes either
+// tile, so blocks never race.
 //
 // Layout and lane mapping are those of the vectorised swizzled tile
 // (tile_vec_kernel.cuh):
@@ -18,6 +20,7 @@
 // skip the lower triangle, so each pair is taken exactly once.
 #include "bounds.cuh"
 #include "launch.cuh"
+#include "ptx.cuh"
 #include "tile_geom.cuh"
 #include "tr_internal.h"
 #include "vec_common.cuh"
@@ -34,8 +37,14 @@ struct InplaceGeom {
     int64_t total;  // batch * tiles * tiles
 };
 
+// Resident blocks per SM the aligned fp32 kernel is compiled for: 6 (40
+// registers, 32 KiB of shared memory each); 0 leaves the others to the compiler.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGeom g) {
+constexpr int kInplaceMinBlocks = VEC && sizeof(T) == 4 ? 6 : 0;
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256, (kInplaceMinBlocks<T, VEC>)) k_inplace(T *__restrict__ data,
+                                                                            InplaceGeom g) {
     constexpr int V = VecTraits<T>::V;
     constexpr int TILE = 16 * V;
     constexpr int LOADS = V;        // 16 tile rows per load pass, TILE rows
@@ -71,71 +80,75 @@ __global__ void __launch_bounds__(256) k_inplace(T *__restrict__ data, InplaceGe
         const int64_t r0 = ti * TILE, c0 = tj * TILE;  // tile (ti, tj); partner at (c0, r0)
         const bool full = r0 + TILE <= g.n && c0 + TILE <= g.n;
 
-        // Phase 1: both tiles, global -> registers -> shared.  fp32 keeps the
-        // loads of both tiles in flight at once (64 registers, 4 blocks/SM);
-        // bf16 tiles are twice the bytes, so the second tile is loaded after
-        // the first is staged (80 registers and 3 blocks/SM instead of 109 and
-        // 2; 2.4% faster on 16384x16384 bf16, 0.6% slower for fp32).
-        // The bf16 order also makes Nsight count 8-13% extra shared wavefronts
-        // (none with both tiles loaded first): cycles lost while the second
-        // tile's loads return, not a conflict of the swizzled layout.
-        constexpr bool SEQUENTIAL = sizeof(T) == 2;
-        Chunk x0[LOADS], x1[SEQUENTIAL ? 1 : LOADS];
-        auto load = [&](int64_t rr0, int64_t cc0, Chunk (&ld)[LOADS]) {
-            const int64_t gc = cc0 + lcc * V;
-#pragma unroll
-            for (int k = 0; k < LOADS; ++k) {
-                const int64_t gr = rr0 + lr + 16 * k;
-                if (VEC && (full || (gr < g.n && gc + V <= g.n))) {
-                    const T *p = plane + gr * g.ld + gc;
-                    ld[k].v = TR_LOAD_OK(side, p, 16) ? *reinterpret_cast<const uint4 *>(p)
-                                                      : make_uint4(0u, 0u, 0u, 0u);
-                } else {
-                    T e[V];
-#pragma unroll
-                    for (int q = 0; q < V; ++q)
-                        e[q] = (gr < g.n && gc + q < g.n &&
-                                TR_LOAD_OK(side, plane + gr * g.ld + gc + q, int(sizeof(T))))
-                                   ? plane[gr * g.ld + gc + q]
-                                   : T(0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if constexpr (sizeof(T) == 4)
-                            ld[k].w[q] = uint32_t(e[q]);
-                        else
-                            ld[k].w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
-                    }
-                }
-            }
-        };
-        if constexpr (SEQUENTIAL) {
-            load(r0, c0, x0);
+        // Phase 1: both tiles into shared memory.  Whole tiles on a 16-byte
+        // aligned side go straight from global memory into their swizzled
+        // slots with asynchronous 16-byte copies, so no register holds data
+        // in flight and the transpose phase sets the register budget (fp32:
+        // 6 blocks/SM instead of 4 with both tiles' loads in registers).  Edge
+        // tiles and misaligned sides go through registers, the second tile's
+        // loads after the first tile is staged.
+        if (VEC && full) {
             if (!first) __syncthreads();  // previous pair fully read from shared memory
             first = false;
 #pragma unroll
             for (int k = 0; k < LOADS; ++k) {
                 const int r = lr + 16 * k;
-                tile0[r * 16 + (lcc ^ ((r / V) & 7))] = x0[k].v;
+                const T *p = plane + (r0 + r) * g.ld + c0 + lcc * V;
+                if (TR_LOAD_OK(side, p, 16)) ptx::cp_async_16(tile0 + r * 16 + (lcc ^ ((r / V) & 7)), p);
             }
-            asm volatile("" ::: "memory");  // keep the second tile's loads after these stores
             if (!diag) {
-                load(c0, r0, x0);
 #pragma unroll
                 for (int k = 0; k < LOADS; ++k) {
                     const int r = lr + 16 * k;
-                    tile1[r * 16 + (lcc ^ ((r / V) & 7))] = x0[k].v;
+                    const T *p = plane + (c0 + r) * g.ld + r0 + lcc * V;
+                    if (TR_LOAD_OK(side, p, 16)) ptx::cp_async_16(tile1 + r * 16 + (lcc ^ ((r / V) & 7)), p);
                 }
             }
+            ptx::cp_async_wait_all();
         } else {
-            load(r0, c0, x0);
-            if (!diag) load(c0, r0, x1);
+            Chunk x0[LOADS];
+            auto load = [&](int64_t rr0, int64_t cc0) {
+                const int64_t gc = cc0 + lcc * V;
+#pragma unroll
+                for (int k = 0; k < LOADS; ++k) {
+                    const int64_t gr = rr0 + lr + 16 * k;
+                    if (VEC && gr < g.n && gc + V <= g.n) {
+                        const T *p = plane + gr * g.ld + gc;
+                        x0[k].v = TR_LOAD_OK(side, p, 16) ? *reinterpret_cast<const uint4 *>(p)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        T e[V];
+#pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            e[q] = (gr < g.n && gc + q < g.n &&
+                                    TR_LOAD_OK(side, plane + gr * g.ld + gc + q, int(sizeof(T))))
+                                       ? plane[gr * g.ld + gc + q]
+                                       : T(0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if constexpr (sizeof(T) == 4)
+                                x0[k].w[q] = uint32_t(e[q]);
+                            else
+                                x0[k].w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                        }
+                    }
+                }
+            };
+            auto stage = [&](uint4 *tile) {
+#pragma unroll
+                for (int k = 0; k < LOADS; ++k) {
+                    const int r = lr + 16 * k;
+                    tile[r * 16 + (lcc ^ ((r / V) & 7))] = x0[k].v;
+                }
+            };
+            load(r0, c0);
             if (!first) __syncthreads();  // previous pair fully read from shared memory
             first = false;
-#pragma unroll
-            for (int k = 0; k < LOADS; ++k) {
-                const int r = lr + 16 * k;
-                tile0[r * 16 + (lcc ^ ((r / V) & 7))] = x0[k].v;
-                if (!diag) tile1[r * 16 + (lcc ^ ((r / V) & 7))] = x1[k].v;
+            stage(tile0);
+            if (!diag) {
+                asm volatile("" ::: "memory");  // keep the second tile's loads after these stores
+                load(c0, r0);
+                stage(tile1);
             }
         }
         __syncthreads();  // every read of both tiles is in before any write
