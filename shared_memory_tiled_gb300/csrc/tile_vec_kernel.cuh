@@ -95,8 +95,19 @@ __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int
 template <typename T, bool VEC_IN>
 constexpr bool kRealignInput = !VEC_IN && sizeof(T) == 2;
 
+// Resident blocks per SM that the bf16 shifted-store shapes AUTO takes (128x128 on 256
+// threads, 64x128 on 128 threads) are compiled for: 64 registers, 4 and 8 blocks instead
+// of 3 and 6 at the compiler's 80.  The price is a few spilled words (16-68 bytes per
+// thread); measured on 16384x16384 bf16, output pitch 16385: 5516 -> 5567 GB/s, both
+// pitches 16385: 4505 -> 4702.  0 leaves every other instantiation to the compiler.
+template <typename T, int MR, int MC, int NT, bool SHIFT_OUT, bool PREFETCH>
+constexpr int kMinBlocks =
+    SHIFT_OUT && !PREFETCH && sizeof(T) == 2 && MC == 16 && ((NT == 256 && MR == 16) || (NT == 128 && MR == 8))
+        ? 65536 / (NT * 64)
+        : 0;
+
 template <typename T, int MR, int MC, int NT, bool VEC_IN, bool SHIFT_OUT, bool PREFETCH>
-__global__ void __launch_bounds__(NT) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
+__global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREFETCH>)) k_tile_vec(const T *__restrict__ in, T *__restrict__ out,
                                                  Geometry g, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     constexpr int TR = V * MR, TC = V * MC;  // tile rows / columns in elements

@@ -67,8 +67,12 @@ def test_shifted_store_tile_budget(vec_report):
     # 64 registers keep 4 blocks of 256 threads per SM
     k = _find(vec_report, "k_tile_vecIjLi32ELi16ELi256ELb1ELb1ELb0E")  # C3's 128x64 tile
     assert k["regs"] <= 64 and k["spill"] == 0
+    # bf16 shifted stores are compiled for 64 registers (4 blocks of 256 / 8 of 128
+    # threads per SM) at the price of a few spilled words
     k = _find(vec_report, "k_tile_vecItLi16ELi16ELi256ELb1ELb1ELb0E")  # bf16 128x128, shifted
-    assert k["regs"] <= 88 and k["spill"] == 0
+    assert k["regs"] <= 64 and k["spill"] <= 160
+    k = _find(vec_report, "k_tile_vecItLi8ELi16ELi128ELb0ELb1ELb0E")  # both pitches odd
+    assert k["regs"] <= 64 and k["spill"] <= 64
 
 
 def test_realigned_input_tile_budget(vec_report):
