@@ -9,8 +9,8 @@ own handle.  The cases are the ones whose addresses come from run-time shifts
 and halos -- odd output pitches (shifted stores fed by halo rows), odd input
 pitches (bf16 rows realigned on chip, fp32 widest per-chunk loads), both at
 once -- every variant, the in-place transpose, the copy, the operand-tile stage,
-the bank probe, a replay of the release fuzz sweep's random configurations and
-one case past 2**31 elements.  Each output is compared with the oracle bit for
+the bank probe, a replay of the release fuzz sweep's random configurations,
+every configured workload at full size and one case past 2**31 elements.  Each output is compared with the oracle bit for
 bit, and the record of refused accesses must stay empty."""
 from __future__ import annotations
 
@@ -25,6 +25,7 @@ from fuzz_cases import U16, U32, draw
 from gpu_util import first_mismatch, from_device, gpu_out, mismatch_report, oracle_out, \
     oracle_out_banded, to_device
 from shared_memory_tiled_gb300 import binding as B
+from shared_memory_tiled_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
@@ -208,3 +209,35 @@ def test_beyond_2_31_elements_both_pitches_odd(dlib):
     want = np.full(n_out, 0xFFBE, dtype=np.uint16)
     oracle_out_banded(x_host, want, 1, rows, cols, ld_in, ld_out, 0, 0)
     assert mismatch_report(got, want) == "identical"
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_configured_workloads_full_size(dlib, name):
+    """Every configured workload at full size through AUTO (and the default TMA
+    pipeline where both sides allow it): oracle-exact, nothing refused."""
+    w = W.WORKLOADS[name]
+    x = W.make_input(w)
+    prefill = W.make_output(w)
+    geo = (w.batch, w.rows, w.cols, w.ld_in, w.ld_out, w.sin, w.sout)
+    want = oracle_out(x, prefill, *geo)
+    aligned = (w.ld_in * w.esize) % 16 == 0 and (w.ld_out * w.esize) % 16 == 0
+    for opt in [dict(variant=V.AUTO)] + ([dict(variant=V.TMA)] if aligned else []):
+        got = gpu_out(x, prefill, *geo, lib=dlib, **opt)
+        assert np.array_equal(got, want), f"{name} {opt}: {first_mismatch(got, want)}"
+        _clean(dlib, f"{name} {opt}")
+
+
+@pytest.mark.parametrize("name", ["c2", "c5"])
+def test_inplace_full_size(dlib, name):
+    import oracle
+    import torch
+    w = W.WORKLOADS[name]
+    x = W.make_input(w)
+    want = oracle.transpose_inplace(x.copy(), n=w.rows)
+    buf, ptr = to_device(x)
+    fn = dlib.tr_transpose_inplace_f32 if w.esize == 4 else dlib.tr_transpose_inplace_bf16
+    assert fn(ptr, 1, w.rows, w.ld_in, w.sin, None) == B.Status.OK
+    torch.cuda.synchronize()
+    got = from_device(buf, x.size, 0, x.dtype.type)
+    assert np.array_equal(got, want), f"{name} in place: {first_mismatch(got, want)}"
+    _clean(dlib, f"{name} in place")
