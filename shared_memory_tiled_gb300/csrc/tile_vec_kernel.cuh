@@ -44,10 +44,12 @@
 // between the tile's first column r0 and the row's next 16-byte boundary (the
 // same for every tile of the row), and the tile owns the output columns
 // [r0 + d, r0 + TR + d) -- plus [0, d) in the first tile row -- so every
-// store inside the matrix is a whole aligned chunk: lane A stores its own last
-// V-d elements followed by the first d of micro-block A+1, fetched from lane
-// A+1 with a warp shuffle or, for the last micro-block row, from V extra input
-// rows staged below the tile (the halo).  Single elements remain only at the
+// store inside the matrix is a whole aligned chunk, which draws on V extra
+// input rows staged below the tile (the halo).  fp32: lane A stores its own
+// last V-d elements followed by the first d of micro-block A+1, fetched from
+// lane A+1 with a warp shuffle or, for the last micro-block row, from the
+// halo.  bf16: each lane gathers its aligned chunk from the shared tile, one
+// element per input row, the shift being an offset in shared addresses.  Single elements remain only at the
 // matrix edges (the first d columns, the columns past the last input row).
 // Tiles at the matrix edge use bounds-checked element accesses except where a
 // whole chunk is in range on an aligned side, or (shifted stores) where the
@@ -96,10 +98,11 @@ template <typename T, bool VEC_IN>
 constexpr bool kRealignInput = !VEC_IN && sizeof(T) == 2;
 
 // Resident blocks per SM that the bf16 shifted-store shapes AUTO takes (128x128 on 256
-// threads, 64x128 on 128 threads) are compiled for: 64 registers, 4 and 8 blocks instead
-// of 3 and 6 at the compiler's 80.  The price is a few spilled words (16-68 bytes per
-// thread); measured on 16384x16384 bf16, output pitch 16385: 5516 -> 5567 GB/s, both
-// pitches 16385: 4505 -> 4702.  0 leaves every other instantiation to the compiler.
+// threads, 64x128 on 128 threads) are compiled for: 64 registers, 4 and 8 blocks.  Left
+// free, the compiler keeps the gathered loads of several chunks in flight with up to 126
+// registers.  Measured on 16384x16384 bf16 (GB/s), output pitch 16385 / both pitches
+// 16385: 5916 / 4943 at 64 registers, 5560 / 4543 at 80 (3 and 6 blocks); at 48 the loads
+// spill 100-228 bytes per thread.  0 leaves every other instantiation to the compiler.
 template <typename T, int MR, int MC, int NT, bool SHIFT_OUT, bool PREFETCH>
 constexpr int kMinBlocks =
     SHIFT_OUT && !PREFETCH && sizeof(T) == 2 && MC == 16 && ((NT == 256 && MR == 16) || (NT == 128 && MR == 8))
@@ -370,6 +373,85 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
         __syncthreads();
         if (PREFETCH && tile + gridDim.x < g.total) load_tile(tile + gridDim.x);
 
+        // ---- phase 2, shifted output rows of 16-bit elements, when every
+        // output row segment of the tile is complete (the tile may still stop
+        // short of the last output rows).  Let d be the number of elements from an output row's
+        // column r0 to its next 16-byte boundary: the tile owns the output
+        // columns [r0 + d, r0 + TR + d) of the row (and [0, d) in the first
+        // tile row), i.e. whole aligned chunks, and the chunk at r0 + d + V*A
+        // holds input rows r0 + d + V*A .. + V-1 of the row's input column.
+        // Each lane gathers such a chunk straight from the shared tile, one
+        // element per input row (the halo rows below the tile supply the last
+        // d), so the shift is only an offset in shared addresses.  Lane map per
+        // warp instruction: 8 consecutive chunks A x 4 output rows; each
+        // element read hits bank 4 * (chunk position) + (its word in the
+        // chunk), and the 8 lanes of one output row see 8 distinct chunk
+        // positions (rows V*A.. are V apart and the swizzle XORs row / V), so
+        // the 32 reads fall on 32 distinct banks.  d depends only on the
+        // plane and on the output row's place in its group of V (the tile's
+        // corner moves a row start by multiples of V elements).  4-byte
+        // elements keep the register window of the micro-block phase below:
+        // with whole words to move it costs less than four gathered loads per
+        // chunk (fp32 12289x7919, output pitch 12289: 6778 GB/s against 6540
+        // gathered), while for bf16 the window's byte permutes and the halo
+        // lane's element reads cost more (16384x16384, output pitch 16385:
+        // 5921 gathered against 5567).
+        if constexpr (SHIFT_OUT && sizeof(T) == 2) {
+            if (r0 + TR <= g.rows) {
+                const T *sm = reinterpret_cast<const T *>(smem);
+                const int s0 = int((reinterpret_cast<uintptr_t>(dst) / sizeof(T)) % V);
+                const int L = int(g.ld_out % V);
+                const int k = t & 3, a = (t >> 2) & 7, w = t >> 5;
+                constexpr int ABLK = MR / 8;                  // blocks of 8 chunks per output row
+                constexpr int PAR = V / 4;                    // output rows of a group a lane takes
+                constexpr int STEPS = MC * PAR * ABLK;        // warp steps per tile
+#pragma unroll
+                for (int j = 0; j < STEPS / (NT / 32); ++j) {
+                    const int step = w + (NT / 32) * j;
+                    const int C = step / (PAR * ABLK);
+                    const int par = (step / ABLK) % PAR;
+                    const int A = (step % ABLK) * 8 + a;
+                    const int cl = PAR * k + par;         // output row within the group of V
+                    const int64_t orow = c0 + V * C + cl;
+                    if (!full && orow >= g.cols) continue;
+                    const int s = (s0 + cl * L) % V, d = (V - s) % V;
+                    T e[V];
+#pragma unroll
+                    for (int q = 0; q < V; ++q) {
+                        const int r = V * A + d + q;  // tile row (the halo from TR on)
+                        e[q] = sm[(r * MC + (C ^ ((r / V) & 7))) * V + cl];
+                    }
+                    Chunk v;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (sizeof(T) == 4)
+                            v.w[q] = uint32_t(e[q]);
+                        else
+                            v.w[q] = uint32_t(e[2 * q]) | (uint32_t(e[2 * q + 1]) << 16);
+                    }
+                    T *row = dst + orow * g.ld_out;
+                    const int64_t wc = r0 + V * A + d;  // first column of the aligned chunk
+                    if (wc + V <= g.rows) {
+                        st16(row + wc, v.v);
+                    } else {
+                        // the halo ran past the last input row
+#pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            if (wc + q < g.rows && TR_STORE_OK(out_side, row + wc + q, int(sizeof(T))))
+                                row[wc + q] = e[q];
+                    }
+                    if (tr == 0 && A == 0) {
+                        // columns [0, d): input rows 0 .. d-1
+#pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            if (q < d && TR_STORE_OK(out_side, row + q, int(sizeof(T))))
+                                row[q] = sm[(q * MC + C) * V + cl];
+                    }
+                }
+                continue;
+            }
+        }
+
         // ---- phase 2: micro-blocks -> registers -> transpose -> global
 #pragma unroll
         for (int j = 0; j < MB; ++j) {
@@ -383,7 +465,7 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
             if (full && !SHIFT_OUT) {
 #pragma unroll
                 for (int m = 0; m < V; ++m) st16(dst + (c0 + V * C + m) * g.ld_out + oc, y[m].v);
-            } else if (SHIFT_OUT && r0 + TR <= g.rows) {
+            } else if (SHIFT_OUT && sizeof(T) == 4 && r0 + TR <= g.rows) {
                 // Every output row segment of the tile is complete (the tile may
                 // still stop short of the last output rows).  For an output row
                 // whose first 16-byte boundary lies d elements past column r0,

@@ -34,14 +34,14 @@ WORD = 4
 def passes(byte_addrs, width=4):
     """Shared-memory passes for one warp instruction in which lane i accesses
     ``width`` bytes at ``byte_addrs[i]`` (None = inactive lane)."""
-    lanes_per_phase = {4: 32, 8: 16, 16: 8}[width]
+    lanes_per_phase = {2: 32, 4: 32, 8: 16, 16: 8}[width]
     total = 0
     for p0 in range(0, 32, lanes_per_phase):
         words_in_bank = defaultdict(set)
         for a in byte_addrs[p0:p0 + lanes_per_phase]:
             if a is None:
                 continue
-            for w in range(a // WORD, (a + width) // WORD):
+            for w in range(a // WORD, max(a // WORD + 1, (a + width) // WORD)):
                 words_in_bank[w % BANKS].add(w)
         total += max((len(s) for s in words_in_bank.values()), default=0)
     return total
@@ -49,7 +49,7 @@ def passes(byte_addrs, width=4):
 
 def conflict_degree(byte_addrs, width=4):
     """Passes divided by the conflict-free minimum (1 = conflict-free)."""
-    minimum = {4: 1, 8: 2, 16: 4}[width]
+    minimum = {2: 1, 4: 1, 8: 2, 16: 4}[width]
     return passes(byte_addrs, width) / minimum
 
 
@@ -189,3 +189,35 @@ def sgemm_as_store(BK, a_stride, j, offset=0):
 def a_stride(BM, BK):
     """The page's padding rule: BM + (32 / BK) % 8 ("The Fix Is One Constant")."""
     return BM + (32 // BK) % 8
+
+
+# --- the bf16 shifted stores' column gather (tile_vec_kernel.cuh) -------------------------
+
+def gather_reads(V, MR, MC, NT, s0, L):
+    """Byte addresses of the column gather's shared reads, one list of 32 per
+    warp instruction: warp w, step j, element q.  Lane (k = lane % 4, a =
+    (lane / 4) % 8) of step `step` reads input row V*A + d + q of column
+    V*C + cl of the swizzled tile (row pitch MC chunks, chunk cc of row r at
+    position cc ^ ((r / V) % 8)), with C, the parity and the block of 8 chunks
+    taken from the step and d the output row's offset to its next 16-byte
+    boundary, fixed by the plane offset s0 and the pitch residue L.  Also
+    returns the largest tile row read."""
+    esize = 16 // V
+    PAR, ABLK = V // 4, MR // 8
+    steps = MC * PAR * ABLK
+    out, max_row = [], 0
+    for w in range(NT // 32):
+        for j in range(steps // (NT // 32)):
+            step = w + (NT // 32) * j
+            C, par, blk = step // (PAR * ABLK), (step // ABLK) % PAR, step % ABLK
+            for q in range(V):
+                addrs = []
+                for lane in range(32):
+                    k, a = lane & 3, (lane >> 2) & 7
+                    cl, A = PAR * k + par, blk * 8 + a
+                    d = (V - (s0 + cl * L) % V) % V
+                    r = V * A + d + q
+                    max_row = max(max_row, r)
+                    addrs.append(((r * MC + (C ^ ((r // V) & 7))) * V + cl) * esize)
+                out.append(addrs)
+    return out, max_row

@@ -130,3 +130,29 @@ def test_rotated_reads_of_the_register_store_pipelines_are_conflict_free(V):
     plain = [(V * (lane & 7) + 0) * 128 + (((lane >> 3) ^ ((V * (lane & 7)) & 7)) << 4)
              for lane in range(32)]
     assert BM.conflict_degree(plain, 16) > 1
+
+
+@pytest.mark.parametrize("MR,NT", [(16, 256), (8, 128)])
+def test_bf16_column_gather_is_conflict_free_and_in_range(MR, NT):
+    """The bf16 shifted stores gather each aligned output chunk from the shared
+    tile one element per input row: every warp instruction's 32 element reads
+    fall on 32 distinct banks for every plane offset and pitch residue, and no
+    read goes past the V halo rows below the tile."""
+    V, MC = 8, 16
+    for s0 in range(V):
+        for L in range(V):
+            reads, max_row = BM.gather_reads(V, MR, MC, NT, s0, L)
+            assert max_row < V * MR + V
+            for addrs in reads:
+                assert BM.conflict_degree(addrs, width=2) == 1, (s0, L)
+
+
+def test_same_gather_for_fp32_would_also_be_conflict_free():
+    # fp32 keeps the register window (faster there), but the lane map itself
+    # is conflict-free for 4-byte elements too
+    for s0 in range(4):
+        for L in range(4):
+            reads, max_row = BM.gather_reads(4, 32, 16, 256, s0, L)
+            assert max_row < 4 * 32 + 4
+            assert all(BM.conflict_degree(a, width=4) == 1 for a in reads)
+

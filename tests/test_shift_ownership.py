@@ -8,6 +8,10 @@ element stores and skip the first d columns.  Lane A of a micro-block row
 writes the aligned chunk made of its own last V-d elements and the first d of
 micro-block A+1 (the halo rows below the tile for the last lane).
 
+The bf16 kernel gathers each aligned chunk from the shared tile instead (input
+rows r0 + d + V*A .. of the output row's column), which is the same column
+ownership and the same source rows.
+
 The model below restates that rule and checks, for every row count, tile
 height, element width and row offset in range, that each output column is
 written exactly once and from the input row it must come from.
