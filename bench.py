@@ -21,8 +21,9 @@ Prints ONE JSON line on rank 0:
   roofline    the transpose kernel against the measured HBM copy peak;
   copy        tr_copy on the same byte count, timed the same way (the ceiling);
   per_config  (default run) every configuration -- c1 index-valued and
-              uniform, c2, c3, c4, c5 -- measured the same way, each with its
-              own copy ceiling, roofline fraction and clock record;
+              uniform, c2, c3, c4, c5 -- then the misaligned-pitch cases
+              and c2 / c5 transposed in place, measured the same way, each
+              with its own copy ceiling, roofline fraction and clock record;
   e2e         the same metric with the host->device copy of the input (pinned)
               and the device->host copy of the output inside every step, next
               to what the host link moves on its own;
@@ -348,8 +349,11 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------ GPU arm
 
-# The configurations measured side by side in the default run (``per_config``).
+# The configurations measured side by side in the default run (``per_config``),
+# then the misaligned-pitch cases and the in-place transpose of the square ones.
 PER_CONFIG = ("c1_index", "c1_uniform", "c2", "c3", "c4", "c5")
+PER_CONFIG_EXTRA = ("c3_back", "c5_oddin", "c5_oddout", "c5_oddboth", "c2_oddout")
+PER_CONFIG_INPLACE = ("c2", "c5")
 
 
 def gbps(nbytes, ms):
@@ -560,7 +564,7 @@ def config_entry(m, peak, inplace=False):
     w = m.w
     e = {
         "workload": w.name + ("_inplace" if inplace else ""),
-        "description": W.DESCRIPTION[w.name],
+        "description": W.DESCRIPTION[w.name] + (", transposed in place" if inplace else ""),
         "bytes_per_step": w.algorithmic_bytes,
         "variant": "INPLACE" if inplace else m.planned.name,
         "value": round(m.value, 2), "unit": "GB/s", "statistic": "median of passes",
@@ -738,12 +742,17 @@ def run_ours(args):
     # ---- every configuration of the workload set, measured the same way
     entries = []
     if per_config:
-        for name in PER_CONFIG:
+        for name in PER_CONFIG + PER_CONFIG_EXTRA:
             if name == w.name:
                 entries.append(head)
                 continue
             mc = measure(gpu, W.WORKLOADS[name], B.make_options(B.Variant.AUTO))
             entries.append(config_entry(mc, peak))
+            del mc
+            torch.cuda.empty_cache()
+        for name in PER_CONFIG_INPLACE:
+            mc = measure(gpu, W.WORKLOADS[name], B.make_options(B.Variant.AUTO), inplace=True)
+            entries.append(config_entry(mc, peak, inplace=True))
             del mc
             torch.cuda.empty_cache()
     gpu.sampler.stop()
@@ -848,7 +857,8 @@ def main(argv=None):
     ap.add_argument("--per-config", dest="per_config", choices=["auto", "on", "off"],
                     default="auto",
                     help="also measure every configuration (c1_index, c1_uniform, c2, c3, c4, "
-                         "c5) with AUTO; auto = only for the default workload and options")
+                         "c5), the misaligned-pitch cases and c2 / c5 in place with AUTO; "
+                         "auto = only for the default workload and options")
     ap.add_argument("--e2e-streams", dest="e2e_streams", type=int, default=3,
                     help="streams (and buffer sets) the end-to-end steps rotate over")
     ap.add_argument("--clock-window", dest="clock_window", type=float, default=0.5,
