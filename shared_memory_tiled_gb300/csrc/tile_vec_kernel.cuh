@@ -41,16 +41,17 @@
 // four 4-byte loads, single elements for bf16 rows 2 bytes past a word.  With
 // SHIFT_OUT the output rows need not start on 16-byte boundaries (e.g. a row
 // pitch of 12289 fp32).  For each output row, d is the number of elements
-// between the tile's first column r0 and the row's next 16-byte boundary (the
-// same for every tile of the row), and the tile owns the output columns
-// [r0 + d, r0 + TR + d) -- plus [0, d) in the first tile row -- so every
-// store inside the matrix is a whole aligned chunk, which draws on V extra
-// input rows staged below the tile (the halo).  fp32: lane A stores its own
-// last V-d elements followed by the first d of micro-block A+1, fetched from
-// lane A+1 with a warp shuffle or, for the last micro-block row, from the
-// halo.  bf16: each lane gathers its aligned chunk from the shared tile, one
-// element per input row, the shift being an offset in shared addresses.  Single elements remain only at the
-// matrix edges (the first d columns, the columns past the last input row).
+// between the tile's first column r0 and the row's next 16-byte boundary
+// (32-byte for bf16 tiles of 128 rows or more; the same for every tile of the
+// row), and the tile owns the output columns [r0 + d, r0 + TR + d) -- plus
+// [0, d) in the first tile row -- so every store inside the matrix is a whole
+// aligned chunk, which draws on V (2V) extra input rows staged below the tile
+// (the halo).  fp32: lane A stores its own last V-d elements followed by the first
+// d of micro-block A+1, fetched from lane A+1 with a warp shuffle or, for the
+// last micro-block row, from the halo.  bf16: each lane gathers its aligned
+// chunk from the shared tile, one element per input row, the shift being an
+// offset in shared addresses.  Single elements remain only at the matrix edges
+// (the first d columns, the columns past the last input row).
 // Tiles at the matrix edge use bounds-checked element accesses except where a
 // whole chunk is in range on an aligned side, or (shifted stores) where the
 // tile's output row segments are complete and only its last output rows are
@@ -97,6 +98,20 @@ __device__ __forceinline__ uint4 window(const Chunk &own, const Chunk &next, int
 template <typename T, bool VEC_IN>
 constexpr bool kRealignInput = !VEC_IN && sizeof(T) == 2;
 
+// Shifted stores: the granule (elements) whose boundaries a tile's owned output
+// columns start on, and the input rows staged below the tile (the halo) to
+// fill them.  bf16 tiles of 128 rows or more own 32-byte runs, so that every
+// 128-byte store of a lane group covers whole 32-byte sectors (a store that
+// splits sectors costs about 4% of the rate; see phase 2); their 2V halo rows
+// add 12.5% to the rows a tile reads.  Shorter bf16 tiles and fp32 tiles own
+// 16-byte runs (a 16-row halo on a 64-row tile costs more than it saves:
+// 16384x16384 bf16 with both pitches 16385 on 64x128 tiles, 5039 GB/s with
+// 16-byte runs against 4668 with 32-byte runs).
+template <typename T, int MR>
+constexpr int kShiftGranule = (sizeof(T) == 2 && MR >= 16 ? 2 : 1) * VecTraits<T>::V;
+template <typename T, int MR, bool SHIFT_OUT>
+constexpr int kHalo = SHIFT_OUT ? kShiftGranule<T, MR> : 0;
+
 // Resident blocks per SM that the bf16 shifted-store shapes AUTO takes (128x128 on 256
 // threads, 64x128 on 128 threads) are compiled for: 64 registers, 4 and 8 blocks.  Left
 // free, the compiler keeps the gathered loads of several chunks in flight with up to 126
@@ -119,10 +134,11 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
     constexpr int LOADS = TR / RPP;          // chunks each thread loads
     static_assert(MR >= 8 && MR <= 32 && MC >= 8 && NT % MC == 0 && (MR * MC) % NT == 0,
                   "unsupported tile shape");
-    // With shifted stores the tile also stages the V input rows below it (the
-    // halo): the last lane of each micro-block row builds its output chunks
-    // from them (phase 2).
-    constexpr int HALO = SHIFT_OUT ? V : 0;       // extra tile rows
+    // With shifted stores the tile also stages the input rows below it (the
+    // halo): the output chunks past its last micro-block row draw on them
+    // (phase 2).
+    constexpr int SG = kShiftGranule<T, MR>;      // shift granule, elements
+    constexpr int HALO = kHalo<T, MR, SHIFT_OUT>; // extra tile rows
     constexpr int HCH = HALO * MC;                // halo chunks
     constexpr int HL = SHIFT_OUT ? (HCH + NT - 1) / NT : 1;  // halo chunks per thread
     // Misaligned input rows of 16-bit elements in a tile that lies wholly
@@ -375,32 +391,36 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
 
         // ---- phase 2, shifted output rows of 16-bit elements, when every
         // output row segment of the tile is complete (the tile may still stop
-        // short of the last output rows).  Let d be the number of elements from an output row's
-        // column r0 to its next 16-byte boundary: the tile owns the output
-        // columns [r0 + d, r0 + TR + d) of the row (and [0, d) in the first
-        // tile row), i.e. whole aligned chunks, and the chunk at r0 + d + V*A
+        // short of the last output rows).  Let d be the number of elements from
+        // an output row's column r0 to its next boundary of SG elements (32
+        // bytes for tiles of 128 rows or more, else 16; d < SG): the tile owns
+        // the output columns [r0 + d, r0 + TR + d) of the row (and [0, d) in the
+        // first tile row), i.e. whole aligned chunks (whose runs of 8 start on
+        // 32-byte sector boundaries when SG = 2V), and the chunk at r0 + d + V*A
         // holds input rows r0 + d + V*A .. + V-1 of the row's input column.
-        // Each lane gathers such a chunk straight from the shared tile, one
-        // element per input row (the halo rows below the tile supply the last
-        // d), so the shift is only an offset in shared addresses.  Lane map per
-        // warp instruction: 8 consecutive chunks A x 4 output rows; each
-        // element read hits bank 4 * (chunk position) + (its word in the
-        // chunk), and the 8 lanes of one output row see 8 distinct chunk
-        // positions (rows V*A.. are V apart and the swizzle XORs row / V), so
-        // the 32 reads fall on 32 distinct banks.  d depends only on the
-        // plane and on the output row's place in its group of V (the tile's
-        // corner moves a row start by multiples of V elements).  4-byte
-        // elements keep the register window of the micro-block phase below:
-        // with whole words to move it costs less than four gathered loads per
-        // chunk (fp32 12289x7919, output pitch 12289: 6778 GB/s against 6540
-        // gathered), while for bf16 the window's byte permutes and the halo
-        // lane's element reads cost more (16384x16384, output pitch 16385:
-        // 5921 gathered against 5567).
+        // (With 16-byte boundaries instead, every 128-byte store run splits two
+        // sectors: 16384x16384 bf16 transposed with the aligned path into an
+        // output pitch of 16392 runs at 6573 GB/s, at 16400 at 6878.)  Each lane
+        // gathers its chunk straight from the shared tile, one element per
+        // input row (the SG halo rows below the tile supply the last d), so the
+        // shift is only an offset in shared addresses.  Lane map per warp
+        // instruction: 8 consecutive chunks A x 4 output rows; each element
+        // read hits bank 4 * (chunk position) + (its word in the chunk), and
+        // the 8 lanes of one output row see 8 distinct chunk positions (rows
+        // V*A.. are V apart and the swizzle XORs row / V), so the 32 reads fall
+        // on 32 distinct banks.  d depends only on the plane and on the output
+        // row's place in its group of SG (the tile's corner moves a row start
+        // by multiples of SG elements).  4-byte elements keep the register
+        // window of the micro-block phase below: with whole words to move it
+        // costs less than four gathered loads per chunk (fp32 12289x7919,
+        // output pitch 12289: 6778 GB/s against 6540 gathered), while for bf16
+        // the window's byte permutes and the halo lane's element reads cost
+        // more (16384x16384, output pitch 16385: 5921 gathered against 5567).
         if constexpr (SHIFT_OUT && sizeof(T) == 2) {
             if (r0 + TR <= g.rows) {
                 const T *sm = reinterpret_cast<const T *>(smem);
-                const int s0 = int((reinterpret_cast<uintptr_t>(dst) / sizeof(T)) % V);
-                const int L = int(g.ld_out % V);
+                const int s0 = int((reinterpret_cast<uintptr_t>(dst) / sizeof(T)) % SG);
+                const int L = int(g.ld_out % SG);
                 const int k = t & 3, a = (t >> 2) & 7, w = t >> 5;
                 constexpr int ABLK = MR / 8;                  // blocks of 8 chunks per output row
                 constexpr int PAR = V / 4;                    // output rows of a group a lane takes
@@ -414,7 +434,8 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
                     const int cl = PAR * k + par;         // output row within the group of V
                     const int64_t orow = c0 + V * C + cl;
                     if (!full && orow >= g.cols) continue;
-                    const int s = (s0 + cl * L) % V, d = (V - s) % V;
+                    // row start offset within its granule (c0 is a multiple of SG)
+                    const int s = (s0 + (V * C + cl) * L) % SG, d = (SG - s) % SG;
                     T e[V];
 #pragma unroll
                     for (int q = 0; q < V; ++q) {
@@ -443,9 +464,9 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
                     if (tr == 0 && A == 0) {
                         // columns [0, d): input rows 0 .. d-1
 #pragma unroll
-                        for (int q = 0; q < V; ++q)
+                        for (int q = 0; q < SG; ++q)
                             if (q < d && TR_STORE_OK(out_side, row + q, int(sizeof(T))))
-                                row[q] = sm[(q * MC + C) * V + cl];
+                                row[q] = sm[(q * MC + (C ^ ((q / V) & 7))) * V + cl];
                     }
                 }
                 continue;
@@ -537,8 +558,8 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
                         int64_t lo = 0;
                         if constexpr (SHIFT_OUT) {
                             if (tr > 0) {
-                                const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % V);
-                                lo = r0 + (V - s) % V;
+                                const int s = int((reinterpret_cast<uintptr_t>(row + r0) / sizeof(T)) % SG);
+                                lo = r0 + (SG - s) % SG;
                             }
                         }
 #pragma unroll
@@ -563,8 +584,8 @@ cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     // The tile (+ halo rows), or when misaligned input rows are realigned on
     // chip the staging rows of MC + 1 chunks, whichever is larger.
-    constexpr size_t tile_chunks = size_t(V * MR + (SO ? V : 0)) * MC;
-    constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR + (SO ? V : 0)) * (MC + 1) : 0;
+    constexpr size_t tile_chunks = size_t(V * MR + kHalo<T, MR, SO>) * MC;
+    constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR + kHalo<T, MR, SO>) * (MC + 1) : 0;
     constexpr size_t smem = (tile_chunks > raw_chunks ? tile_chunks : raw_chunks) * 16;
     auto kern = k_tile_vec<T, MR, MC, NT, VI, SO, PF>;
     // Resident blocks per SM on each device; 0 = not set up on that device yet.

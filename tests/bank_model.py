@@ -199,9 +199,10 @@ def gather_reads(V, MR, MC, NT, s0, L):
     (lane / 4) % 8) of step `step` reads input row V*A + d + q of column
     V*C + cl of the swizzled tile (row pitch MC chunks, chunk cc of row r at
     position cc ^ ((r / V) % 8)), with C, the parity and the block of 8 chunks
-    taken from the step and d the output row's offset to its next 16-byte
-    boundary, fixed by the plane offset s0 and the pitch residue L.  Also
-    returns the largest tile row read."""
+    taken from the step and d the output row's offset to its next granule
+    boundary, fixed by the plane offset s0 and the pitch residue L (both
+    modulo the shift granule G: 2V elements, 32 bytes, for bf16 tiles of 128
+    rows or more, else V).  Also returns the largest tile row read."""
     esize = 16 // V
     PAR, ABLK = V // 4, MR // 8
     steps = MC * PAR * ABLK
@@ -215,7 +216,8 @@ def gather_reads(V, MR, MC, NT, s0, L):
                 for lane in range(32):
                     k, a = lane & 3, (lane >> 2) & 7
                     cl, A = PAR * k + par, blk * 8 + a
-                    d = (V - (s0 + cl * L) % V) % V
+                    G = 2 * V if V == 8 and MR >= 16 else V   # shift granule
+                    d = (G - (s0 + (V * C + cl) * L) % G) % G
                     r = V * A + d + q
                     max_row = max(max_row, r)
                     addrs.append(((r * MC + (C ^ ((r // V) & 7))) * V + cl) * esize)

@@ -137,12 +137,14 @@ def test_bf16_column_gather_is_conflict_free_and_in_range(MR, NT):
     """The bf16 shifted stores gather each aligned output chunk from the shared
     tile one element per input row: every warp instruction's 32 element reads
     fall on 32 distinct banks for every plane offset and pitch residue, and no
-    read goes past the V halo rows below the tile."""
+    read goes past the halo rows below the tile (one granule: 2V rows for
+    tiles of 128 rows or more, else V)."""
     V, MC = 8, 16
-    for s0 in range(V):
-        for L in range(V):
+    G = 2 * V if MR >= 16 else V  # shift granule (halo rows)
+    for s0 in range(G):
+        for L in range(G):
             reads, max_row = BM.gather_reads(V, MR, MC, NT, s0, L)
-            assert max_row < V * MR + V
+            assert max_row < V * MR + G
             for addrs in reads:
                 assert BM.conflict_degree(addrs, width=2) == 1, (s0, L)
 
