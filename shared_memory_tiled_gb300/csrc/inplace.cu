@@ -16,8 +16,12 @@
 // chunk position cc ^ ((r / V) % 8), 256 threads, 16-byte loads and stores and a
 // register micro-transpose; VEC = false moves single elements (any alignment).
 //
-// Blocks walk a batch * T * T grid of tile coordinates (T tiles per side) and
-// skip the lower triangle, so each pair is taken exactly once.
+// Blocks walk the pairs (ti <= tj) of each plane's upper triangle of tiles (T
+// tiles per side, T (T + 1) / 2 pairs), tile column by tile column: pair index
+// tj (tj + 1) / 2 + ti.  Walking the whole T x T grid and letting the blocks
+// below the diagonal exit at once costs a launch slot per skipped block:
+// 8192x8192 fp32 in place runs at 6330 GB/s that way against 6427 with the
+// triangle, 16384x16384 bf16 at 6331 against 6483.
 #include "bounds.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -34,15 +38,40 @@ namespace {
 struct InplaceGeom {
     int64_t batch, n, ld, stride;
     int64_t tiles;  // tiles per side
-    int64_t total;  // batch * tiles * tiles
+    int64_t pairs;  // tile pairs per plane: tiles * (tiles + 1) / 2
+    int64_t total;  // batch * pairs
 };
+
+// Pair index p (< tiles * (tiles + 1) / 2) -> tiles (ti <= tj), p = tj (tj + 1) / 2 + ti.
+// tj is the floor of the root of x (x + 1) / 2 = p, taken in float.  For p < 2^32
+// (tj < 92682) the float root is within 0.02 of the true one, so one step up or
+// down corrects it, in 32-bit arithmetic (every triangular number compared with
+// p stays below 2^32; halving the even factor first keeps the product there too).
+__device__ __forceinline__ uint32_t triangle32(uint32_t n) {
+    return (n & 1u) ? n * ((n + 1u) >> 1) : (n >> 1) * (n + 1u);
+}
+__device__ __forceinline__ void split_pair32(uint32_t p, uint32_t &ti, uint32_t &tj) {
+    tj = uint32_t((sqrtf(8.0f * float(p) + 1.0f) - 1.0f) * 0.5f);
+    tj -= triangle32(tj) > p ? 1u : 0u;
+    tj += triangle32(tj + 1u) <= p ? 1u : 0u;
+    ti = p - triangle32(tj);
+}
+// Any size: the same root, corrected by as many steps as it takes.
+__device__ __forceinline__ void split_pair64(int64_t p, int64_t &ti, int64_t &tj) {
+    tj = int64_t((sqrtf(8.0f * float(p) + 1.0f) - 1.0f) * 0.5f);
+    while (tj > 0 && tj * (tj + 1) / 2 > p) --tj;
+    while ((tj + 1) * (tj + 2) / 2 <= p) ++tj;
+    ti = p - tj * (tj + 1) / 2;
+}
 
 // Resident blocks per SM the aligned fp32 kernel is compiled for: 6 (40
 // registers, 32 KiB of shared memory each); 0 leaves the others to the compiler.
 template <typename T, bool VEC>
 constexpr int kInplaceMinBlocks = VEC && sizeof(T) == 4 ? 6 : 0;
 
-template <typename T, bool VEC>
+// BIG: more than 2^32 tile pairs in the launch (64-bit pair arithmetic, kept
+// out of the common instantiations, whose registers it would raise).
+template <typename T, bool VEC, bool BIG>
 __global__ void __launch_bounds__(256, (kInplaceMinBlocks<T, VEC>)) k_inplace(T *__restrict__ data,
                                                                             InplaceGeom g) {
     constexpr int V = VecTraits<T>::V;
@@ -60,21 +89,19 @@ __global__ void __launch_bounds__(256, (kInplaceMinBlocks<T, VEC>)) k_inplace(T 
 
     bool first = true;
     for (int64_t w = blockIdx.x; w < g.total; w += gridDim.x) {
-        const int64_t per_plane = g.tiles * g.tiles;
         int64_t b, ti, tj;
-        if (g.total <= 0xFFFFFFFFll) {  // 32-bit division is far cheaper than 64-bit
-            const uint32_t w32 = uint32_t(w), pp = uint32_t(per_plane), t32 = uint32_t(g.tiles);
-            const uint32_t bb = w32 / pp, rem = w32 - bb * pp, i = rem / t32;
+        if constexpr (!BIG) {  // 32-bit arithmetic is far cheaper than 64-bit
+            const uint32_t w32 = uint32_t(w), pp = uint32_t(g.pairs);
+            const uint32_t bb = w32 / pp;
+            uint32_t i, j;
+            split_pair32(w32 - bb * pp, i, j);
             b = bb;
             ti = i;
-            tj = rem - i * t32;
+            tj = j;
         } else {
-            b = w / per_plane;
-            const int64_t rem = w - b * per_plane;
-            ti = rem / g.tiles;
-            tj = rem - ti * g.tiles;
+            b = w / g.pairs;
+            split_pair64(w - b * g.pairs, ti, tj);
         }
-        if (ti > tj) continue;  // the pair is handled at (tj, ti)
         T *plane = data + b * g.stride;
         const bool diag = ti == tj;
         const int64_t r0 = ti * TILE, c0 = tj * TILE;  // tile (ti, tj); partner at (c0, r0)
@@ -181,11 +208,11 @@ __global__ void __launch_bounds__(256, (kInplaceMinBlocks<T, VEC>)) k_inplace(T 
     }
 }
 
-template <typename T, bool VEC>
-cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
+template <typename T, bool VEC, bool BIG>
+cudaError_t launch_one(T *data, const InplaceGeom &g, cudaStream_t stream) {
     constexpr int V = VecTraits<T>::V;
     constexpr size_t smem = 2 * size_t(16 * V) * 16 * 16;
-    auto kern = k_inplace<T, VEC>;
+    auto kern = k_inplace<T, VEC, BIG>;
     if (smem > 48 * 1024) {
         static std::atomic<bool> opted[64];  // per device, zero-initialised (static)
         static std::mutex mu;
@@ -205,6 +232,12 @@ cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
     return launch_pdl(kern, dim3(grid_blocks(g.total)), dim3(256), smem, stream, data, g);
 }
 
+template <typename T, bool VEC>
+cudaError_t launch_typed(T *data, const InplaceGeom &g, cudaStream_t stream) {
+    return g.total <= 0xFFFFFFFFll ? launch_one<T, VEC, false>(data, g, stream)
+                                   : launch_one<T, VEC, true>(data, g, stream);
+}
+
 }  // namespace
 
 // Debug builds: this unit's record of refused accesses.
@@ -213,9 +246,10 @@ TR_BOUNDS_READER(read_bounds_inplace)
 cudaError_t launch_inplace(void *data, int esize, int64_t batch, int64_t n, int64_t ld,
                            int64_t stride, cudaStream_t stream) {
     const int V = 16 / esize;
-    InplaceGeom g{batch, n, ld, stride, 0, 0};
+    InplaceGeom g{batch, n, ld, stride, 0, 0, 0};
     g.tiles = (n + 16 * V - 1) / (16 * V);
-    g.total = batch * g.tiles * g.tiles;
+    g.pairs = g.tiles * (g.tiles + 1) / 2;
+    g.total = batch * g.pairs;
     const bool vec = side_aligned16(data, ld, stride, batch, esize);
     if (esize == 4)
         return vec ? launch_typed<uint32_t, true>(static_cast<uint32_t *>(data), g, stream)
