@@ -34,8 +34,8 @@
 //
 // Misaligned sides.  With VEC_IN = false (input rows need not start on
 // 16-byte boundaries) bf16 tiles that lie wholly inside the matrix read every
-// row segment as the aligned 16-byte chunks covering it, stage them unshifted
-// in shared memory and cut each thread's chunk out of two neighbours; all
+// row segment as the aligned 16-byte chunks covering it and cut each thread's
+// chunk out of its own and the next (the next lane's, by a warp shuffle); all
 // other chunks whose elements are in range (fp32, edge tiles) are loaded with
 // the widest accesses their own address allows -- one 16-byte, two 8-byte or
 // four 4-byte loads, single elements for bf16 rows 2 bytes past a word.  With
@@ -144,9 +144,9 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
     // Misaligned input rows of 16-bit elements in a tile that lies wholly
     // inside the matrix, halo rows included: each row segment is read as the
     // aligned 16-byte chunks that cover it -- MC by the row's own threads, one
-    // more past its end by a helper thread -- staged as they are with a row
-    // pitch of MC + 1 chunks, and every thread then cuts its chunk's elements
-    // out of its own aligned chunk and the next one.  The extra bytes those
+    // more past its end by a helper thread, staged in shared memory past the
+    // tile -- and every thread then cuts its chunk's elements out of its own
+    // aligned chunk and the next one.  The extra bytes those
     // chunks hold belong to the input's own extent (neighbouring columns,
     // pitch padding, the row before or after) except in two tiles, which take
     // the per-chunk path: the first tile of the first plane, whose first chunk
@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
     // row's end, whose last aligned chunk may reach past the input.
     constexpr bool RAW = kRealignInput<T, VEC_IN>;
     constexpr int XL = RAW ? (TR + HALO + NT - 1) / NT : 1;  // extra chunks per thread
-    constexpr int RP = MC + 1;                               // staging row pitch, chunks
-    extern __shared__ uint4 smem[];  // TR + HALO rows of MC chunks, or of RP
+    static_assert(!RAW || (32 % MC == 0 || MC % 32 == 0), "a row's lanes share a warp");
+    static_assert(!RAW || ((HALO * MC) % NT == 0 || (HALO * MC) % 32 == 0), "halo lanes fill whole warps");
+    extern __shared__ uint4 smem[];  // TR + HALO rows of MC chunks (+ one chunk per row when RAW)
 
     pdl_prologue();
     const int t = threadIdx.x;
@@ -320,26 +321,20 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
         if (!PREFETCH) load_tile(tile);
         if (tile != blockIdx.x) __syncthreads();  // previous tile fully read
         if (RAW && raw_tile(full, b, tr, tc)) {
-            // Realign: stage the aligned chunks unshifted, then take elements
-            // s .. s+V-1 of (own chunk, next chunk), s being the row's offset
-            // from its 16-byte boundary.  Both shared passes are conflict-free
-            // (8 lanes of a phase touch 8 consecutive chunks, and the helper
-            // rows' last chunks lie RP = 1 mod 8 chunks apart).
-#pragma unroll
-            for (int k = 0; k < LOADS; ++k) smem[(lr + RPP * k) * RP + lcc] = ld[k].v;
-            if constexpr (SHIFT_OUT) {
-#pragma unroll
-                for (int k = 0; k < HL; ++k) {
-                    const int h = t + NT * k;
-                    if (HCH % NT != 0 && h >= HCH) continue;
-                    smem[(TR + h / MC) * RP + h % MC] = hl[k].v;
-                }
-            }
+            // Realign: each thread takes elements s .. s+V-1 of (own chunk,
+            // next chunk), s being the row's offset from its 16-byte boundary.
+            // The next chunk is the next lane's own (a warp shuffle), except
+            // for a row's last lane, which takes the chunk past the segment
+            // that the helper thread of that row staged in shared memory past
+            // the tile (consecutive lanes, consecutive 16-byte slots: no
+            // conflicts).  The tile's own chunks never go through shared
+            // memory unshifted.
+            uint4 *ext = smem + (TR + HALO) * MC;  // one chunk per tile (and halo) row
 #pragma unroll
             for (int k = 0; k < XL; ++k) {
                 const int rr = t + NT * k;
                 if ((TR + HALO) % NT != 0 && rr >= TR + HALO) continue;
-                smem[rr * RP + MC] = xl[k].v;
+                ext[rr] = xl[k].v;
             }
             __syncthreads();
             // Byte offsets from 16-byte boundaries: row lr's, and the step to
@@ -351,13 +346,15 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
             for (int k = 0; k < LOADS; ++k) {
                 const int sh = int(((a0 + uint32_t(k) * step) & 15u) / sizeof(T));
                 Chunk nb;
-                nb.v = smem[(lr + RPP * k) * RP + lcc + 1];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) nb.w[q] = __shfl_down_sync(0xffffffffu, ld[k].w[q], 1);
+                if (lcc == MC - 1) nb.v = ext[lr + RPP * k];
                 ld[k].v = window<T>(ld[k], nb, sh);
             }
             if constexpr (SHIFT_OUT) {
 #pragma unroll
                 for (int k = 0; k < HL; ++k) {
-                    const int h = t + NT * k;
+                    const int h = t + NT * k;  // whole warps run past HCH (it is a multiple of 32)
                     if (HCH % NT != 0 && h >= HCH) continue;
                     const int r = TR + h / MC;
                     const int sh = int((reinterpret_cast<uintptr_t>(
@@ -365,11 +362,12 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
                                         15u) /
                                        sizeof(T));
                     Chunk nb;
-                    nb.v = smem[r * RP + h % MC + 1];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) nb.w[q] = __shfl_down_sync(0xffffffffu, hl[k].w[q], 1);
+                    if (h % MC == MC - 1) nb.v = ext[r];
                     hl[k].v = window<T>(hl[k], nb, sh);
                 }
             }
-            __syncthreads();  // staging read before the tile overwrites it
         }
         // Phase 1b: registers -> swizzled shared tile.
 #pragma unroll
@@ -583,7 +581,7 @@ template <typename T, int MR, int MC, int NT, bool VI, bool SO, bool PF>
 cudaError_t launch_one(const Problem &p, bool diagonal) {
     constexpr int V = VecTraits<T>::V;
     // The tile (+ halo rows), or when misaligned input rows are realigned on
-    // chip the staging rows of MC + 1 chunks, whichever is larger.
+    // chip the tile plus one staged chunk per row.
     constexpr size_t tile_chunks = size_t(V * MR + kHalo<T, MR, SO>) * MC;
     constexpr size_t raw_chunks = kRealignInput<T, VI> ? size_t(V * MR + kHalo<T, MR, SO>) * (MC + 1) : 0;
     constexpr size_t smem = (tile_chunks > raw_chunks ? tile_chunks : raw_chunks) * 16;

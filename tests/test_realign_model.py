@@ -5,8 +5,10 @@ When input rows do not start on 16-byte boundaries, a tile that lies wholly
 inside the matrix (with shifted stores, its halo rows below included) reads
 each of its row segments as the aligned 16-byte chunks that cover it: thread lcc the chunk holding its first element, and a helper
 thread the chunk past the segment's end when the row is not aligned.  Every
-thread then takes elements s .. s+V-1 of (its chunk, the next chunk), s being
-the row's element offset from its 16-byte boundary, which the kernel derives
+thread then takes elements s .. s+V-1 of (its chunk, the next chunk: the next
+lane's own by a warp shuffle, or for a row's last lane the helper's chunk staged
+in shared memory), s being the row's element offset from its 16-byte boundary,
+which the kernel derives
 from the low 32 bits of one row address and a per-row step.  Two tiles take the
 per-chunk path instead: the first tile of the first plane, and a tile in the
 last plane reading the last input row whose row segments end fewer than V
