@@ -160,6 +160,24 @@ def test_output_pitch_not_a_multiple_of_16_bytes(dtype):
             check(x, prefill, geo, **kw)
 
 
+def test_bf16_shifted_stores_every_32_byte_offset():
+    """bf16 tiles of 128 rows own output runs that start on 32-byte boundaries:
+    with an odd output pitch the rows' offsets cover every residue modulo 16
+    elements (heads of up to 15 elements in the first tile row), and shifting
+    the output base moves them all; exact and ragged last tile rows (the
+    bounds-checked path past the last full tile row), a ragged tile column and
+    batched planes with a plane pitch that shifts them again."""
+    for (b, r, c, po, pp) in [(1, 384, 150, 1, 0), (1, 421, 150, 3, 0), (2, 256, 136, 5, 3),
+                              (1, 143, 300, 15, 0), (3, 128, 70, 9, 7)]:
+        x, prefill, geo = case(U16, b, r, c, 0, po, pp, seed=r + c + po)
+        for out_off in (0, 1, 5, 8, 13):
+            for kw in [dict(variant=V.AUTO), dict(variant=V.TILE_VEC, tile_rows=128, tile_cols=128),
+                       dict(variant=V.TILE_VEC, threads=128, tile_rows=64, tile_cols=128)]:
+                check(x, prefill, geo, out_off=out_off, **kw)
+            # and with the input rows misaligned too (realigned loads + shifted stores)
+            check(x, prefill, geo, in_off=3, out_off=out_off, variant=V.AUTO)
+
+
 def test_unsupported_vector_tile_shape_is_refused():
     x, prefill, geo = case(U32, 1, 64, 64)
     with pytest.raises(B.TransposeError) as e:
