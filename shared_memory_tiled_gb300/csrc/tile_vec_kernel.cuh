@@ -402,11 +402,17 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
         // gathers its chunk straight from the shared tile, one element per
         // input row (the SG halo rows below the tile supply the last d), so the
         // shift is only an offset in shared addresses.  Lane map per warp
-        // instruction: 8 consecutive chunks A x 4 output rows; each element
-        // read hits bank 4 * (chunk position) + (its word in the chunk), and
-        // the 8 lanes of one output row see 8 distinct chunk positions (rows
-        // V*A.. are V apart and the swizzle XORs row / V), so the 32 reads fall
-        // on 32 distinct banks.  d depends only on the plane and on the output
+        // instruction: RUN consecutive chunks A of KL = 32 / RUN output rows,
+        // the rows' elements in distinct words of the chunk; RUN = 16 where the
+        // tile has 16 chunks per output row segment, so that a warp stores
+        // 256-byte runs, else 8.  Each element read hits bank 4 * (chunk
+        // position) + (its word in the chunk), and 8 lanes of one output row
+        // see 8 distinct chunk positions (rows V*A.. are V apart and the
+        // swizzle XORs row / V): with RUN = 8 the 32 reads fall on 32 distinct
+        // banks, with RUN = 16 two lanes share each bank (2 wavefronts per
+        // read).  The longer store runs win: 16384x16384 bf16 with output pitch
+        // 16385 runs at 6330 GB/s with RUN = 16 against 6195 with RUN = 8
+        // (conflict-free).  d depends only on the plane and on the output
         // row's place in its group of SG (the tile's corner moves a row start
         // by multiples of SG elements).  4-byte elements keep the register
         // window of the micro-block phase below: with whole words to move it
@@ -419,16 +425,18 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
                 const T *sm = reinterpret_cast<const T *>(smem);
                 const int s0 = int((reinterpret_cast<uintptr_t>(dst) / sizeof(T)) % SG);
                 const int L = int(g.ld_out % SG);
-                const int k = t & 3, a = (t >> 2) & 7, w = t >> 5;
-                constexpr int ABLK = MR / 8;                  // blocks of 8 chunks per output row
-                constexpr int PAR = V / 4;                    // output rows of a group a lane takes
+                constexpr int RUN = MR >= 16 ? 16 : 8;        // consecutive chunks of a row per instruction
+                constexpr int KL = 32 / RUN;                  // output rows per instruction
+                constexpr int PAR = V / KL;                   // output rows of a group a lane takes
+                const int k = t % KL, a = (t / KL) % RUN, w = t >> 5;
+                constexpr int ABLK = MR / RUN;                // runs per output row segment
                 constexpr int STEPS = MC * PAR * ABLK;        // warp steps per tile
 #pragma unroll
                 for (int j = 0; j < STEPS / (NT / 32); ++j) {
                     const int step = w + (NT / 32) * j;
                     const int C = step / (PAR * ABLK);
                     const int par = (step / ABLK) % PAR;
-                    const int A = (step % ABLK) * 8 + a;
+                    const int A = (step % ABLK) * RUN + a;
                     const int cl = PAR * k + par;         // output row within the group of V
                     const int64_t orow = c0 + V * C + cl;
                     if (!full && orow >= g.cols) continue;

@@ -195,18 +195,24 @@ def a_stride(BM, BK):
 
 def gather_reads(V, MR, MC, NT, s0, L):
     """Byte addresses of the column gather's shared reads, one list of 32 per
-    warp instruction: warp w, step j, element q.  Lane (k = lane % 4, a =
-    (lane / 4) % 8) of step `step` reads input row V*A + d + q of column
+    warp instruction: warp w, step j, element q.  Lane (k = lane % KL, a =
+    (lane / KL) % RUN) of step `step` reads input row V*A + d + q of column
     V*C + cl of the swizzled tile (row pitch MC chunks, chunk cc of row r at
-    position cc ^ ((r / V) % 8)), with C, the parity and the block of 8 chunks
-    taken from the step and d the output row's offset to its next granule
-    boundary, fixed by the plane offset s0 and the pitch residue L (both
-    modulo the shift granule G: 2V elements, 32 bytes, for bf16 tiles of 128
-    rows or more, else V).  Also returns the largest tile row read."""
+    position cc ^ ((r / V) % 8)), RUN being the consecutive chunks A of one
+    output row an instruction covers (16 when the tile has them, else 8), KL =
+    32 / RUN its output rows, cl = (V / KL) k + par, with C, the parity par and
+    the run taken from the step and d the output row's offset to its next
+    granule boundary, fixed by the plane offset s0 and the pitch residue L
+    (both modulo the shift granule G: 2V elements, 32 bytes, for tiles of 128
+    rows or more, else V).  Also returns the largest tile row read and the
+    (C, cl, A) chunks stored, one entry per lane and step."""
     esize = 16 // V
-    PAR, ABLK = V // 4, MR // 8
+    RUN = 16 if MR >= 16 else 8
+    KL = 32 // RUN
+    PAR, ABLK = V // KL, MR // RUN
+    G = 2 * V if V * MR >= 128 else V   # shift granule
     steps = MC * PAR * ABLK
-    out, max_row = [], 0
+    out, max_row, stored = [], 0, []
     for w in range(NT // 32):
         for j in range(steps // (NT // 32)):
             step = w + (NT // 32) * j
@@ -214,12 +220,13 @@ def gather_reads(V, MR, MC, NT, s0, L):
             for q in range(V):
                 addrs = []
                 for lane in range(32):
-                    k, a = lane & 3, (lane >> 2) & 7
-                    cl, A = PAR * k + par, blk * 8 + a
-                    G = 2 * V if V == 8 and MR >= 16 else V   # shift granule
+                    k, a = lane % KL, (lane // KL) % RUN
+                    cl, A = PAR * k + par, blk * RUN + a
                     d = (G - (s0 + (V * C + cl) * L) % G) % G
                     r = V * A + d + q
                     max_row = max(max_row, r)
                     addrs.append(((r * MC + (C ^ ((r // V) & 7))) * V + cl) * esize)
+                    if q == 0:
+                        stored.append((C, cl, A))
                 out.append(addrs)
-    return out, max_row
+    return out, max_row, stored

@@ -133,28 +133,32 @@ def test_rotated_reads_of_the_register_store_pipelines_are_conflict_free(V):
 
 
 @pytest.mark.parametrize("MR,NT", [(16, 256), (8, 128)])
-def test_bf16_column_gather_is_conflict_free_and_in_range(MR, NT):
+def test_bf16_column_gather_banks_range_and_coverage(MR, NT):
     """The bf16 shifted stores gather each aligned output chunk from the shared
-    tile one element per input row: every warp instruction's 32 element reads
-    fall on 32 distinct banks for every plane offset and pitch residue, and no
-    read goes past the halo rows below the tile (one granule: 2V rows for
-    tiles of 128 rows or more, else V)."""
+    tile one element per input row.  With 8 chunks of an output row per warp
+    instruction (64-row tiles) the 32 element reads fall on 32 distinct banks;
+    with 16 (128-row tiles, 256-byte store runs) two lanes share each bank.
+    That holds for every plane offset and pitch residue; no read goes past the
+    halo rows below the tile (one granule: 2V rows for tiles of 128 rows or
+    more, else V), and the lanes store every chunk of the tile exactly once."""
     V, MC = 8, 16
-    G = 2 * V if MR >= 16 else V  # shift granule (halo rows)
+    G = 2 * V if MR >= 16 else V
     for s0 in range(G):
         for L in range(G):
-            reads, max_row = BM.gather_reads(V, MR, MC, NT, s0, L)
+            reads, max_row, stored = BM.gather_reads(V, MR, MC, NT, s0, L)
             assert max_row < V * MR + G
-            for addrs in reads:
-                assert BM.conflict_degree(addrs, width=2) == 1, (s0, L)
+            worst = max(BM.conflict_degree(addrs, width=2) for addrs in reads)
+            assert worst == (2 if MR >= 16 else 1), (s0, L)
+            want = {(C, cl, A) for C in range(MC) for cl in range(V) for A in range(MR)}
+            assert len(stored) == len(want) and set(stored) == want
 
 
-def test_same_gather_for_fp32_would_also_be_conflict_free():
-    # fp32 keeps the register window (faster there), but the lane map itself
-    # is conflict-free for 4-byte elements too
+def test_same_gather_for_fp32_would_also_be_conflict_free_on_64_row_tiles():
+    # fp32 keeps the register window (faster there), but the 8-chunk lane map
+    # itself is conflict-free for 4-byte elements too
     for s0 in range(4):
         for L in range(4):
-            reads, max_row = BM.gather_reads(4, 32, 16, 256, s0, L)
-            assert max_row < 4 * 32 + 4
+            reads, max_row, _ = BM.gather_reads(4, 8, 16, 128, s0, L)
+            assert max_row < 4 * 8 + 4
             assert all(BM.conflict_degree(a, width=4) == 1 for a in reads)
 
