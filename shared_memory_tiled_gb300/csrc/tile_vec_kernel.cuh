@@ -100,9 +100,9 @@ constexpr bool kRealignInput = !VEC_IN && sizeof(T) == 2;
 
 // Shifted stores: the granule (elements) whose boundaries a tile's owned output
 // columns start on, and the input rows staged below the tile (the halo) to
-// fill them.  bf16 tiles of 128 rows or more own 32-byte runs, so that every
-// 128-byte store of a lane group covers whole 32-byte sectors (a store that
-// splits sectors costs about 4% of the rate; see phase 2); their 2V halo rows
+// fill them.  bf16 tiles of 128 rows or more own 32-byte runs, so that a
+// warp's store runs cover whole 32-byte sectors (a store run that splits
+// sectors costs about 4% of the rate; see phase 2); their 2V halo rows
 // add 12.5% to the rows a tile reads.  Shorter bf16 tiles and fp32 tiles own
 // 16-byte runs (a 16-row halo on a 64-row tile costs more than it saves:
 // 16384x16384 bf16 with both pitches 16385 on 64x128 tiles, 5039 GB/s with
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(NT, (kMinBlocks<T, MR, MC, NT, SHIFT_OUT, PREF
         // an output row's column r0 to its next boundary of SG elements (32
         // bytes for tiles of 128 rows or more, else 16; d < SG): the tile owns
         // the output columns [r0 + d, r0 + TR + d) of the row (and [0, d) in the
-        // first tile row), i.e. whole aligned chunks (whose runs of 8 start on
+        // first tile row), i.e. whole aligned chunks (whose store runs start on
         // 32-byte sector boundaries when SG = 2V), and the chunk at r0 + d + V*A
         // holds input rows r0 + d + V*A .. + V-1 of the row's input column.
         // (With 16-byte boundaries instead, every 128-byte store run splits two
