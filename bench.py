@@ -490,7 +490,8 @@ def measure(gpu, w, opts, inplace=False):
     m.x_host = W.make_input(w)
     m.pin_in = torch.from_numpy(m.x_host.view(ndt)).pin_memory()
     m.d_in = torch.empty(w.in_elems, dtype=m.tdt, device=gpu.dev)
-    m.d_out = torch.empty(w.out_elems, dtype=m.tdt, device=gpu.dev)
+    # in place there is no output buffer (and no out-of-place plan)
+    m.d_out = None if inplace else torch.empty(w.out_elems, dtype=m.tdt, device=gpu.dev)
     m.d_in.copy_(m.pin_in)
     # Rewrite the uploaded input in place with an elementwise kernel (values
     # unchanged), so its pages were last written by SM stores, as data made by
@@ -498,15 +499,18 @@ def measure(gpu, w, opts, inplace=False):
     # engine were measured to read up to 4% slower under the transposed
     # access, by an amount that depended on what the GPU had run before.
     m.d_in.add_(0)
-    m.targs = B.make_args(m.d_in.data_ptr(), m.d_out.data_ptr(), dt, w.batch, w.rows, w.cols,
-                          w.ld_in, w.ld_out, w.sin, w.sout, gpu.sptr)
     m.topts = opts
-    plan = B.Plan()
-    B.check(B.tr_plan_ex(m.targs, opts, plan))
-    m.plan = plan
-    m.planned = B.Variant(plan.variant)
+    m.plan = m.planned = m.targs = None
+    if not inplace:
+        m.targs = B.make_args(m.d_in.data_ptr(), m.d_out.data_ptr(), dt, w.batch, w.rows, w.cols,
+                              w.ld_in, w.ld_out, w.sin, w.sout, gpu.sptr)
+        plan = B.Plan()
+        B.check(B.tr_plan_ex(m.targs, opts, plan))
+        m.plan = plan
+        m.planned = B.Variant(plan.variant)
     ex = gpu.lib.tr_transpose_ex
-    pa, po = ctypes.byref(m.targs), ctypes.byref(opts)
+    pa = ctypes.byref(m.targs) if m.targs is not None else None
+    po = ctypes.byref(opts)
     m.po = po
     ipf = gpu.lib.tr_transpose_inplace_f32 if w.esize == 4 else gpu.lib.tr_transpose_inplace_bf16
     m.ipf = ipf
@@ -587,7 +591,7 @@ def config_entry(m, peak, inplace=False):
         "l2": "flushed before every step" if m.flush else "no flush (input and output > L2)",
         "clocks": m.clocks,
     }
-    if m.planned.name == "TILE_VEC" and not inplace:
+    if not inplace and m.planned.name == "TILE_VEC":
         e["tile"] = f"{m.plan.tile_rows}x{m.plan.tile_cols}, {m.plan.threads} threads"
         e["aligned_sides"] = {"input": bool(m.plan.vec_in), "output": bool(m.plan.vec_out)}
     if m.flush:
